@@ -1,0 +1,403 @@
+#!/usr/bin/env python
+"""Benchmark of the sparse MLA training backward on one GB300 (or N replicas).
+
+One step = one full backward (delta, CSR build, S/dP/P/dS, dKV intermediate,
+dq, atomic-free dKV gather, d_sink) through the C ABI on the headline
+workload of the aiter page's Performance table: T=4096, H=128, D=512,
+topk=512, num_kv=5120 (128-row causal window + 384 uniform pool picks),
+synthetic seeded inputs (no dataset exists for it). O and lse come from the
+library's forward (untimed).
+
+Prints ONE JSON line (rank 0). The metric is TFLOPS over the valid
+(token, head, rank) triples at 5 GEMMs x 2 x 512 FLOPs each; ms/call is
+reported next to it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`--impl reference` times the fp64 CPU oracle (the correctness reference) on a
+bounded token slice of the same workload, on the host's cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse-MLA bwd TFLOPS & ms/call (T=4096,H=128,topk=512,D=512) vs BF16 peak"
+WORKLOAD = "headline"
+PAGES_CONTEXT = {"hardware": "AMD MI355X", "bwd_end_to_end_ms": 3.238, "bwd_tflops_nominal": 424}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower() in ("active", "0x1", "1", "yes")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_sample(spec, inp, seconds: float = 12.0):
+    """Times the fp64 oracle backward on a token slice sized to about `seconds`."""
+    import numpy as np
+    import oracle
+    from sparse_mla_attention_gb300 import workloads as W
+
+    kv64 = oracle.bf16_to_f64(inp["kv"])
+    t0 = spec.T // 2
+
+    def run(n):
+        sl = slice(t0, t0 + n)
+        q64 = oracle.bf16_to_f64(inp["q"][sl])
+        do64 = oracle.bf16_to_f64(inp["do"][sl])
+        topk = np.ascontiguousarray(inp["topk"][sl])
+        sink = None if inp["sink"] is None else inp["sink"].astype(np.float64)
+        o64, lse = oracle.fwd(q64, kv64, topk, sink, inp["scale"])
+        o_in = oracle.bf16_to_f64(oracle.f64_to_bf16(o64))
+        lse_in = lse.astype(np.float32).astype(np.float64)
+        t = time.perf_counter()
+        oracle.bwd(q64, kv64, do64, o_in, lse_in, topk, sink, inp["scale"])
+        dt = time.perf_counter() - t
+        return dt, W.flops_valid(topk, spec.H)
+
+    dt, fl = run(4)
+    n = int(max(4, min(spec.T - t0, 4 * seconds / max(dt, 1e-3))))
+    dt, fl = run(n)
+    return {"value": fl / dt / 1e12, "unit": "TFLOPS", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"full fp64 backward (dq, dkv scatter, d_sink) of tokens "
+                      f"{t0}..{t0 + n - 1} of the {spec.name} workload ({dt:.1f} s)",
+            "ms_per_token": dt * 1e3 / n}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from sparse_mla_attention_gb300 import workloads as W
+    import oracle
+    oracle.build()
+    spec = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(spec)
+    per_step = max(2.0, 60.0 / max(args.steps + args.warmup, 1))
+    res = None
+    vals = []
+    for i in range(args.warmup + args.steps):
+        res = cpu_oracle_sample(spec, inp, seconds=per_step)
+        if i >= args.warmup:
+            vals.append(res["value"])
+    value = statistics.median(vals) if vals else res["value"]
+    total_flops = W.flops_valid(inp["topk"], spec.H)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_flops / (value * 1e12) * 1e3 if value > 0 else None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": spec.name, "shape": spec.describe(),
+                   "note": "each step times the fp64 oracle on a bounded token slice; "
+                           "ms_per_step extrapolates to the whole workload"},
+        "cpu_baseline": {"kind": res["kind"], "cores": res["cores"], "sample": res["sample"],
+                         "value": value, "unit": "TFLOPS"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from sparse_mla_attention_gb300 import build as smla_build
+    smla_build.build()
+    import sparse_mla_attention_gb300 as smla
+    from sparse_mla_attention_gb300 import _lib, workloads as W
+
+    spec = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(spec)
+    T, H, K, N = spec.T, spec.H, spec.topk, spec.num_kv
+
+    def dev_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, kv, do = (dev_bf16(inp[k]) for k in ("q", "kv", "do"))
+    topk = torch.from_numpy(inp["topk"]).to(dev)
+    sink = None if inp["sink"] is None else torch.from_numpy(inp["sink"]).to(dev)
+    o, lse = smla.sparse_mla_fwd(q, kv, topk, sink, scale=inp["scale"])
+    r_chunk = spec.r_chunk or None
+    ws = smla.Workspace(dev)
+    dq = torch.empty_like(q)
+    dkv = torch.empty_like(kv)
+    dsink = None if sink is None else torch.empty(H, dtype=torch.float32, device=dev)
+    out = (dq, dkv, dsink)
+
+    def step():
+        smla.sparse_mla_bwd(q, kv, do, o, lse, topk, sink, scale=inp["scale"], r_chunk=r_chunk,
+                            workspace=ws, out=out, check_status=False)
+
+    step()
+    st = smla.device_status(ws.buf)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the first step")
+    for _ in range(args.warmup):
+        step()
+    stream = torch.cuda.current_stream(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    _lib.profiling(True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = e0.elapsed_time(e1)
+    phases = _lib.profile_read()
+    _lib.profiling(False)
+    clk = clocks.stop()
+    ms = elapsed_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    flops = W.flops_valid(inp["topk"], H)
+    flops_nom = W.flops_nominal(T, H, K)
+    value = flops * world / (ms * 1e-3) / 1e12
+    launches = int(sum(p["launches"] for p in phases.values()))
+
+    # ---- end to end: host (pinned) inputs -> device -> backward -> host results
+    e2e = None
+    if not args.no_e2e:
+        host_in = {"q": q.cpu().pin_memory(), "kv": kv.cpu().pin_memory(),
+                   "do": do.cpu().pin_memory(), "o": o.cpu().pin_memory(),
+                   "lse": lse.cpu().pin_memory(), "topk": topk.cpu().pin_memory()}
+        if sink is not None:
+            host_in["sink"] = sink.cpu().pin_memory()
+        host_out = {"dq": torch.empty(dq.shape, dtype=dq.dtype).pin_memory(),
+                    "dkv": torch.empty(dkv.shape, dtype=dkv.dtype).pin_memory()}
+        if dsink is not None:
+            host_out["dsink"] = torch.empty(dsink.shape, dtype=dsink.dtype).pin_memory()
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+        def e2e_step():
+            for k, v in host_in.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            r = smla.sparse_mla_bwd(dev_in["q"], dev_in["kv"], dev_in["do"], dev_in["o"],
+                                    dev_in["lse"], dev_in["topk"], dev_in.get("sink"),
+                                    scale=inp["scale"], r_chunk=r_chunk, workspace=ws,
+                                    check_status=False)
+            host_out["dq"].copy_(r[0], non_blocking=True)
+            host_out["dkv"].copy_(r[1], non_blocking=True)
+            if r[2] is not None:
+                host_out["dsink"].copy_(r[2], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(3, min(args.steps, 10))
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_e2e = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            t = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": flops * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOPS",
+               "ms_per_step": ms_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # ---- roofline of the dominant kernel (live CUDA-event phase times)
+    peaks = _peaks()
+    dom_name, dom = max(phases.items(), key=lambda kv_: kv_[1]["ms"])
+    per_launch_ms = dom["ms"] / max(dom["calls"], 1)
+    roofline = {"kernel": dom_name, "share_of_step": dom["ms"] / max(elapsed_ms, 1e-9)}
+    algo = _algorithmic(dom_name, spec, inp["topk"])
+    if algo["bound"] == "tensor":
+        achieved = algo["flops"] / (per_launch_ms * 1e-3) / 1e12
+        roofline.update({"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                         "peak_source": peaks["source"] + " bf16 burst"})
+    elif algo["bound"] == "alu":
+        achieved = algo["flops"] / (per_launch_ms * 1e-3) / 1e12
+        alu_peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        roofline.update({"bound": "alu", "achieved": achieved, "peak": alu_peak,
+                         "unit": "TFLOP/s", "frac": achieved / alu_peak,
+                         "peak_source": "derived: 152 SMs x 128 fp32 FMA/clk x 2 x max SM clock"})
+    else:
+        achieved = algo["bytes"] / (per_launch_ms * 1e-3) / 1e9
+        roofline.update({"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "peak_source": peaks["source"] + " copy"})
+    roofline["traffic"] = None
+    roofline["per_launch_ms"] = per_launch_ms
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(spec, inp, seconds=args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": spec.name, "shape": spec.describe(),
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (q, dO, O: 1.5 GB)",
+                   "flops_valid_per_step": flops, "flops_nominal_per_step": flops_nom,
+                   "tflops_nominal": flops_nom * world / (ms * 1e-3) / 1e12,
+                   "frac_of_bf16_peak": value / world / peaks["bf16_tflops"]},
+        "phases_ms_per_step": {k: v["ms"] / args.steps for k, v in phases.items()},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "pages_context": PAGES_CONTEXT,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def _algorithmic(phase: str, spec, topk):
+    """Algorithmic work per launch of one phase (FLOPs or bytes)."""
+    from sparse_mla_attention_gb300 import workloads as W
+    T, H, K, N = spec.T, spec.H, spec.topk, spec.num_kv
+    valid = W.valid_ranks(topk)
+    nchunks = K // (spec.r_chunk or K)
+    if phase == "attn_sdi":       # S, dP, interm: 4 of the 5 GEMMs
+        return {"bound": "tensor", "flops": 4 * 2 * 512 * H * valid / nchunks}
+    if phase == "attn_dq":
+        return {"bound": "tensor", "flops": 1 * 2 * 512 * H * valid / nchunks}
+    if phase == "attn":           # CUDA-core path: all five products on FMA units
+        return {"bound": "alu", "flops": 5 * 2 * 512 * H * valid / nchunks}
+    if phase == "delta":
+        return {"bound": "hbm", "bytes": 2 * T * H * 512 * 2 + T * H * 4}
+    if phase == "gather":
+        per = valid / nchunks
+        return {"bound": "hbm", "bytes": per * 512 * 2 + per * 4 + N * 512 * 2}
+    if phase == "csr":
+        per = T * (K // nchunks)
+        return {"bound": "hbm", "bytes": per * 4 * 6}
+    return {"bound": "hbm", "bytes": T * H * 8}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,390 @@
+// smla_api.cu -- the C ABI of libsmla.so: argument validation, workspace
+// plans and the phase sequence of the sparse MLA backward.
+//
+// Phase order follows the aiter page "Sparse MLA training backward"
+// (Structure table): delta, then per rank chunk (R_CHUNK) the CSR build, the
+// dQ / dKV-interm work and the atomic-free dKV gather, then d_sink. The
+// validation rules are the page wrapper's (D == 512, num_kv >= T, shapes),
+// plus the review comments on that page (R_CHUNK must divide topk; dtype and
+// lse shape checks), plus alignment and overlap checks.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "smla_internal.cuh"
+
+namespace smla {
+
+// ------------------------------------------------------------ phase profiler
+namespace prof {
+enum Phase { kDelta, kCsr, kAttn, kGather, kDsink, kFwd, kPhases };
+const char* const kNames[kPhases] = {"delta", "csr", "attn", "gather", "dsink", "fwd"};
+std::atomic<long long> g_launches{0};
+bool g_on = false;
+struct Pending { int phase; cudaEvent_t a, b; long long launches; };
+std::vector<Pending> g_pending;
+std::vector<cudaEvent_t> g_pool;
+double g_ms[kPhases];
+long long g_calls[kPhases], g_kernels[kPhases];
+
+cudaEvent_t take_event() {
+    if (!g_pool.empty()) { cudaEvent_t e = g_pool.back(); g_pool.pop_back(); return e; }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) { cudaGetLastError(); return nullptr; }
+    return e;
+}
+
+void reset() {
+    for (auto& p : g_pending) { g_pool.push_back(p.a); g_pool.push_back(p.b); }
+    g_pending.clear();
+    for (int i = 0; i < kPhases; ++i) { g_ms[i] = 0; g_calls[i] = 0; g_kernels[i] = 0; }
+}
+
+// Brackets one phase with events on the stream while profiling is on.
+struct Scope {
+    int phase; cudaStream_t s; cudaEvent_t a = nullptr; long long l0;
+    Scope(int ph, cudaStream_t st) : phase(ph), s(st), l0(g_launches.load()) {
+        if (g_on && (a = take_event())) cudaEventRecord(a, s);
+    }
+    ~Scope() {
+        if (!a) return;
+        cudaEvent_t b = take_event();
+        if (!b) { g_pool.push_back(a); return; }
+        cudaEventRecord(b, s);
+        g_pending.push_back({phase, a, b, g_launches.load() - l0});
+    }
+};
+}  // namespace prof
+
+void note_launch(int n) { prof::g_launches += n; }
+
+cudaError_t launch_attn_chunk_simt(const ChunkArgs& a, cudaStream_t s);
+
+cudaError_t launch_attn_chunk(const ChunkArgs& a, cudaStream_t s) {
+    return launch_attn_chunk_simt(a, s);
+}
+
+BwdPlan plan_bwd(const smla_dims& d) {
+    BwdPlan p{};
+    p.T = d.T; p.H = d.H; p.K = d.topk; p.N = d.num_kv;
+    p.R = d.r_chunk > 0 ? d.r_chunk : d.topk;
+    p.nchunks = int(p.K / p.R);
+    p.csr = plan_csr(p.T, p.R, p.N);
+    const int64_t nnz_max = p.T * p.R;
+    p.max_segs = (nnz_max + kGatherSeg - 1) / kGatherSeg + p.N;
+    size_t off = kStatusBytes;
+    auto take = [&](size_t bytes) { size_t o = off; off += align_up(bytes > 0 ? bytes : 1, 256); return o; };
+    p.off_delta = take(size_t(p.T * p.H) * 4);
+    p.off_rowptr = take(size_t(p.N + 1) * 4);
+    p.off_col = take(size_t(nnz_max) * 4);
+    p.off_csr = take(p.csr.bytes);
+    p.off_segcnt = take(size_t(p.N) * 4);
+    p.off_segptr = take(size_t(p.N + 1) * 4);
+    p.off_segrow = take(size_t(p.max_segs) * 4);
+    p.off_scan_tmp2 = take(scan_tmp_bytes(p.N));
+    p.off_partial = take(size_t(p.max_segs) * kD * 4);
+    p.off_interm = take(size_t(nnz_max) * kD * 2);
+    p.off_dst = take(size_t(nnz_max) * size_t(p.H) * 2);
+    p.off_dqacc = take(p.nchunks > 1 ? size_t(p.T * p.H) * kD * 4 : 0);
+    p.off_dkvacc = take(p.nchunks > 1 ? size_t(p.N) * kD * 4 : 0);
+    p.bytes = off;
+    return p;
+}
+
+namespace {
+
+int check_dims(const smla_dims* d, bool need_bwd_limits) {
+    if (!d) return SMLA_ERR_NULL;
+    if (d->D != kD) return SMLA_ERR_D512;
+    if (d->T < 0 || d->topk < 1 || d->num_kv < 1) return SMLA_ERR_SHAPE;
+    if (d->H < 16 || d->H > 128 || d->H % 16 != 0) return SMLA_ERR_SHAPE;
+    if (d->num_kv < d->T) return SMLA_ERR_NUM_KV_LT_T;
+    if (int64_t(d->T) * d->topk > int64_t(INT32_MAX)) return SMLA_ERR_SHAPE;
+    if (!std::isfinite(d->scale) || d->scale < 0.f) return SMLA_ERR_ARG;
+    if (need_bwd_limits) {
+        if (d->r_chunk < 0 || d->r_chunk > d->topk) return SMLA_ERR_RCHUNK;
+        if (d->r_chunk > 0 && d->topk % d->r_chunk != 0) return SMLA_ERR_RCHUNK;
+    }
+    return SMLA_OK;
+}
+
+float eff_scale(const smla_dims& d) {
+    return d.scale > 0.f ? d.scale : 1.0f / std::sqrt(float(d.D));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Span { const void* p; size_t n; };
+
+bool overlaps(const Span& a, const Span& b) {
+    if (!a.p || !b.p || a.n == 0 || b.n == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
+// Each output must be disjoint from every other span (inputs, outputs, workspace).
+int check_overlap(const Span* outs, int nout, const Span* ins, int nin) {
+    for (int i = 0; i < nout; ++i) {
+        for (int j = 0; j < nin; ++j)
+            if (overlaps(outs[i], ins[j])) return SMLA_ERR_OVERLAP;
+        for (int j = i + 1; j < nout; ++j)
+            if (overlaps(outs[i], outs[j])) return SMLA_ERR_OVERLAP;
+    }
+    return SMLA_OK;
+}
+
+int check_arch() {
+    static int cached[64];          // 0 unknown, 1 ok, 2 wrong arch
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SMLA_ERR_CUDA; }
+    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev] == 1 ? SMLA_OK : SMLA_ERR_ARCH;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SMLA_ERR_CUDA;
+    }
+    const bool ok = major == 10 && minor == 3;
+    if (dev >= 0 && dev < 64) cached[dev] = ok ? 1 : 2;
+    return ok ? SMLA_OK : SMLA_ERR_ARCH;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace smla
+
+using namespace smla;
+
+extern "C" {
+
+int smla_version(void) { return 100; }
+
+const char* smla_status_string(int code) {
+    switch (code) {
+        case SMLA_OK: return "ok";
+        case SMLA_ERR_NULL: return "a required pointer is NULL";
+        case SMLA_ERR_SHAPE: return "unsupported shape (H must be a multiple of 16 in 16..128; T >= 0; topk, num_kv >= 1; T*topk < 2^31)";
+        case SMLA_ERR_D512: return "D must be 512";
+        case SMLA_ERR_NUM_KV_LT_T: return "num_kv must be >= T";
+        case SMLA_ERR_RCHUNK: return "r_chunk must be 0 or a divisor of topk";
+        case SMLA_ERR_ALIGN: return "every device pointer must be 16-byte aligned";
+        case SMLA_ERR_OVERLAP: return "an output overlaps an input, another output or the workspace";
+        case SMLA_ERR_WORKSPACE: return "workspace missing or smaller than smla_workspace_size()";
+        case SMLA_ERR_ARCH: return "the current device is not compute capability 10.3 (sm_103)";
+        case SMLA_ERR_CUDA: return "a CUDA runtime call failed";
+        case SMLA_ERR_INDEX: return "a topk index outside [-1, num_kv) was seen (treated as masked)";
+        case SMLA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+        case SMLA_ERR_SINK: return "d_sink must be given exactly when sink is given";
+        case SMLA_ERR_ARG: return "invalid argument (scale must be finite and >= 0)";
+        default: return "unknown status code";
+    }
+}
+
+int smla_workspace_size(int op, const smla_dims* dims, size_t* bytes) {
+    if (!bytes) return SMLA_ERR_NULL;
+    if (!dims) return SMLA_ERR_NULL;
+    if (op == SMLA_OP_CSR) {
+        const int64_t R = dims->r_chunk > 0 ? dims->r_chunk : dims->topk;
+        if (dims->T < 0 || dims->topk < 1 || dims->num_kv < 1 || R < 1 || R > dims->topk)
+            return SMLA_ERR_SHAPE;
+        *bytes = kStatusBytes + plan_csr(dims->T, R, dims->num_kv).bytes;
+        return SMLA_OK;
+    }
+    const int rc = check_dims(dims, op == SMLA_OP_BWD);
+    if (rc) return rc;
+    if (op == SMLA_OP_FWD) { *bytes = kStatusBytes; return SMLA_OK; }
+    if (op == SMLA_OP_BWD) { *bytes = plan_bwd(*dims).bytes; return SMLA_OK; }
+    return SMLA_ERR_ARG;
+}
+
+int smla_fwd(const uint16_t* q, const uint16_t* kv, const int32_t* topk, const float* sink,
+             uint16_t* o, float* lse, const smla_dims* dims, void* workspace,
+             size_t workspace_bytes, void* stream) {
+    int rc = check_dims(dims, false);
+    if (rc) return rc;
+    const smla_dims& d = *dims;
+    if (!kv || !workspace) return SMLA_ERR_NULL;
+    if (d.T > 0 && (!q || !topk || !o || !lse)) return SMLA_ERR_NULL;   // NULL allowed when T == 0
+    const void* fptrs[] = {q, kv, topk, sink, o, lse, workspace};
+    for (const void* p : fptrs)
+        if (p && !aligned16(p)) return SMLA_ERR_ALIGN;
+    if (workspace_bytes < kStatusBytes) return SMLA_ERR_WORKSPACE;
+    const size_t thd = size_t(d.T) * d.H * kD * 2;
+    const Span ins[] = {{q, thd}, {kv, size_t(d.num_kv) * kD * 2}, {topk, size_t(d.T) * d.topk * 4},
+                        {sink, sink ? size_t(d.H) * 4 : 0}, {workspace, workspace_bytes}};
+    const Span outs[] = {{o, thd}, {lse, size_t(d.T) * d.H * 4}};
+    if ((rc = check_overlap(outs, 2, ins, 5))) return rc;
+    if (overlaps(Span{workspace, workspace_bytes}, ins[0]) ||
+        overlaps(Span{workspace, workspace_bytes}, ins[1]))
+        return SMLA_ERR_OVERLAP;
+    if ((rc = check_arch())) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned* status = static_cast<unsigned*>(workspace);
+    if ((rc = cuda_rc(cudaMemsetAsync(status, 0, sizeof(unsigned), s)))) return rc;
+    prof::Scope ph(prof::kFwd, s);
+    return cuda_rc(launch_fwd(q, kv, topk, sink, o, lse, d.T, d.H, d.topk, d.num_kv, eff_scale(d),
+                              status, s));
+}
+
+int smla_bwd(const uint16_t* q, const uint16_t* kv, const uint16_t* dO, const uint16_t* o,
+             const float* lse, const int32_t* topk, const float* sink, uint16_t* dq,
+             uint16_t* dkv, float* d_sink, const smla_dims* dims, void* workspace,
+             size_t workspace_bytes, void* stream) {
+    int rc = check_dims(dims, true);
+    if (rc) return rc;
+    const smla_dims& d = *dims;
+    // Pointers to zero-size tensors (T == 0) may be NULL.
+    const bool has_tokens = d.T > 0;
+    if (!kv || !dkv || !workspace) return SMLA_ERR_NULL;
+    if (has_tokens && (!q || !dO || !o || !lse || !topk || !dq)) return SMLA_ERR_NULL;
+    if ((sink == nullptr) != (d_sink == nullptr)) return SMLA_ERR_SINK;
+    const void* ptrs[] = {q, kv, dO, o, lse, topk, sink, dq, dkv, d_sink, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SMLA_ERR_ALIGN;
+    const BwdPlan plan = plan_bwd(d);
+    if (workspace_bytes < plan.bytes) return SMLA_ERR_WORKSPACE;
+    const size_t thd = size_t(d.T) * d.H * kD * 2, th4 = size_t(d.T) * d.H * 4;
+    const Span ins[] = {{q, thd}, {kv, size_t(d.num_kv) * kD * 2}, {dO, thd}, {o, thd},
+                        {lse, th4}, {topk, size_t(d.T) * d.topk * 4},
+                        {sink, sink ? size_t(d.H) * 4 : 0}};
+    const Span outs[] = {{dq, thd}, {dkv, size_t(d.num_kv) * kD * 2},
+                         {d_sink, d_sink ? size_t(d.H) * 4 : 0}, {workspace, workspace_bytes}};
+    if ((rc = check_overlap(outs, 4, ins, 7))) return rc;
+    if ((rc = check_arch())) return rc;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    unsigned* status = reinterpret_cast<unsigned*>(ws);
+    if ((rc = cuda_rc(cudaMemsetAsync(status, 0, sizeof(unsigned), s)))) return rc;
+    if (d.T == 0) {
+        if ((rc = cuda_rc(cudaMemsetAsync(dkv, 0, size_t(d.num_kv) * kD * 2, s)))) return rc;
+        if (d_sink) return cuda_rc(cudaMemsetAsync(d_sink, 0, size_t(d.H) * 4, s));
+        return SMLA_OK;
+    }
+    float* delta = reinterpret_cast<float*>(ws + plan.off_delta);
+    int32_t* row_ptr = reinterpret_cast<int32_t*>(ws + plan.off_rowptr);
+    int32_t* col = reinterpret_cast<int32_t*>(ws + plan.off_col);
+    uint16_t* interm = reinterpret_cast<uint16_t*>(ws + plan.off_interm);
+    uint16_t* dsT = reinterpret_cast<uint16_t*>(ws + plan.off_dst);
+    float* dq_acc = plan.nchunks > 1 ? reinterpret_cast<float*>(ws + plan.off_dqacc) : nullptr;
+    float* dkv_acc = plan.nchunks > 1 ? reinterpret_cast<float*>(ws + plan.off_dkvacc) : nullptr;
+
+    {
+        prof::Scope ph(prof::kDelta, s);
+        if ((rc = cuda_rc(launch_delta(o, dO, delta, int64_t(d.T) * d.H, s)))) return rc;
+    }
+    const float scale = eff_scale(d);
+    for (int c = 0; c < plan.nchunks; ++c) {
+        const int r0 = int(c * plan.R);
+        const bool first = c == 0, last = c == plan.nchunks - 1;
+        {
+            prof::Scope ph(prof::kCsr, s);
+            rc = cuda_rc(launch_csr(topk, d.T, d.topk, r0, int(plan.R), d.num_kv, row_ptr, col,
+                                    ws + plan.off_csr, plan.csr, status, s));
+            if (rc) return rc;
+        }
+        ChunkArgs a{};
+        a.q = q; a.kv = kv; a.dO = dO; a.lse = lse; a.delta = delta; a.topk = topk;
+        a.T = d.T; a.H = d.H; a.K = d.topk; a.N = d.num_kv; a.r0 = r0; a.R = int(plan.R);
+        a.scale = scale; a.interm = interm; a.dsT = dsT; a.dq_acc = dq_acc; a.dq_out = dq;
+        a.first_chunk = first; a.last_chunk = last; a.status = status;
+        {
+            prof::Scope ph(prof::kAttn, s);
+            if ((rc = cuda_rc(launch_attn_chunk(a, s)))) return rc;
+        }
+        prof::Scope ph(prof::kGather, s);
+        rc = cuda_rc(launch_gather(row_ptr, col, interm, d.num_kv, plan.max_segs,
+                                   reinterpret_cast<int32_t*>(ws + plan.off_segcnt),
+                                   reinterpret_cast<int32_t*>(ws + plan.off_segptr),
+                                   reinterpret_cast<int32_t*>(ws + plan.off_segrow),
+                                   ws + plan.off_scan_tmp2,
+                                   reinterpret_cast<float*>(ws + plan.off_partial), dkv_acc, dkv,
+                                   first, last, s));
+        if (rc) return rc;
+    }
+    if (sink) {
+        prof::Scope ph(prof::kDsink, s);
+        if ((rc = cuda_rc(launch_dsink(delta, lse, sink, d_sink, d.T, d.H, s)))) return rc;
+    }
+    return SMLA_OK;
+}
+
+int smla_csr_build(const int32_t* topk, int32_t T, int32_t topk_w, int32_t r0, int32_t r_len,
+                   int32_t num_kv, int32_t* row_ptr, int32_t* col, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+    if (!row_ptr || !workspace) return SMLA_ERR_NULL;
+    if (T > 0 && (!topk || !col)) return SMLA_ERR_NULL;        // NULL allowed when T == 0
+    if (T < 0 || topk_w < 1 || num_kv < 1 || r0 < 0 || r_len < 1 ||
+        int64_t(r0) + r_len > topk_w || int64_t(T) * topk_w > int64_t(INT32_MAX))
+        return SMLA_ERR_SHAPE;
+    if ((topk && !aligned16(topk)) || !aligned16(row_ptr) || (col && !aligned16(col)) ||
+        !aligned16(workspace))
+        return SMLA_ERR_ALIGN;
+    const CsrPlan plan = plan_csr(T, r_len, num_kv);
+    if (workspace_bytes < kStatusBytes + plan.bytes) return SMLA_ERR_WORKSPACE;
+    const Span ins[] = {{topk, size_t(T) * topk_w * 4}};
+    const Span outs[] = {{row_ptr, size_t(num_kv + 1) * 4}, {col, size_t(T) * r_len * 4},
+                         {workspace, workspace_bytes}};
+    int rc = check_overlap(outs, 3, ins, 1);
+    if (rc) return rc;
+    if ((rc = check_arch())) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    unsigned* status = reinterpret_cast<unsigned*>(ws);
+    if ((rc = cuda_rc(cudaMemsetAsync(status, 0, sizeof(unsigned), s)))) return rc;
+    return cuda_rc(launch_csr(topk, T, topk_w, r0, r_len, num_kv, row_ptr, col, ws + kStatusBytes,
+                              plan, status, s));
+}
+
+int smla_profiling(int enable) {
+    prof::reset();
+    prof::g_on = enable != 0;
+    return SMLA_OK;
+}
+
+int smla_profile_read(smla_phase_stat* out, int max, int* n) {
+    if (!n) return SMLA_ERR_NULL;
+    int rc = SMLA_OK;
+    for (auto& p : prof::g_pending) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(p.b) != cudaSuccess || cudaEventElapsedTime(&ms, p.a, p.b) != cudaSuccess) {
+            cudaGetLastError();
+            rc = SMLA_ERR_CUDA;
+        }
+        prof::g_ms[p.phase] += ms;
+        prof::g_calls[p.phase] += 1;
+        prof::g_kernels[p.phase] += p.launches;
+        prof::g_pool.push_back(p.a);
+        prof::g_pool.push_back(p.b);
+    }
+    prof::g_pending.clear();
+    int k = 0;
+    for (int i = 0; i < prof::kPhases; ++i) {
+        if (prof::g_calls[i] == 0) continue;
+        if (out && k < max)
+            out[k] = smla_phase_stat{prof::kNames[i], prof::g_ms[i], prof::g_calls[i], prof::g_kernels[i]};
+        ++k;
+    }
+    *n = k;
+    return rc;
+}
+
+int smla_get_device_status(const void* workspace, void* stream, int* status) {
+    if (!workspace || !status) return SMLA_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) { cudaGetLastError(); return SMLA_ERR_CUDA; }
+    unsigned bits = 0;
+    if (cudaMemcpy(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return SMLA_ERR_CUDA;
+    }
+    *status = SMLA_OK;
+    if (bits & (1u << SMLA_ERR_INDEX)) *status = SMLA_ERR_INDEX;
+    else if (bits & (1u << SMLA_ERR_TIMEOUT)) *status = SMLA_ERR_TIMEOUT;
+    else if (bits) *status = SMLA_ERR_CUDA;
+    return SMLA_OK;
+}
+
+}  // extern "C"

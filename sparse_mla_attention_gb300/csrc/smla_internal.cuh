@@ -1,0 +1,126 @@
+// smla_internal.cuh -- declarations shared by the CUDA translation units of
+// libsmla.so (device helpers, workspace carving, kernel launchers).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/smla.h"
+
+namespace smla {
+
+constexpr int kD = 512;                 // head width fixed by the contract
+constexpr int kWarp = 32;
+
+// ---------------------------------------------------------------- status word
+// The first 256 bytes of every workspace hold a status word: bit `code` is
+// set when a kernel meets the condition of that code (SMLA_ERR_INDEX,
+// SMLA_ERR_TIMEOUT). The host clears it at the start of each call.
+constexpr size_t kStatusBytes = 256;
+
+__device__ __forceinline__ void flag_status(unsigned* status, int code) {
+    atomicOr(status, 1u << code);
+}
+
+// Reads topk[t, r] and classifies it: returns the row index, or -1 for a
+// masked slot. Indices outside [-1, num_kv) are reported and treated as masked.
+__device__ __forceinline__ int load_index(const int32_t* p, int num_kv, unsigned* status) {
+    int j = __ldg(p);
+    if (j < -1 || j >= num_kv) {
+        flag_status(status, SMLA_ERR_INDEX);
+        j = -1;
+    }
+    return j;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// Two floats -> packed bf16x2 (round to nearest even); `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ------------------------------------------------------------ workspace plans
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Radix-sort based CSR build parameters.
+constexpr int kRadixBits = 11;
+constexpr int kRadixBuckets = 1 << kRadixBits;   // 2048
+constexpr int kRadixWarps = 8;
+constexpr int kRadixPerWarp = 1024;
+constexpr int kRadixBlock = kRadixWarps * kRadixPerWarp;  // entries per radix block
+
+// dKV gather: a kv row's contributor list is cut into segments of at most
+// kGatherSeg entries; each segment is summed on its own and the segments of a
+// row are then added in order.
+constexpr int kGatherSeg = 256;
+
+struct CsrPlan {
+    int64_t n;          // entries T * r_len
+    int nblk;           // radix blocks
+    int passes;         // radix passes
+    int64_t nscan;      // counters per pass (buckets * nblk)
+    size_t off_keys0, off_vals0, off_keys1, off_vals1, off_cnt, off_scan_tmp;
+    size_t bytes;       // scratch bytes (excluding row_ptr / col)
+};
+
+CsrPlan plan_csr(int64_t T, int64_t r_len, int64_t num_kv);
+
+struct BwdPlan {
+    int64_t T, H, K, N, R;   // R = rank chunk
+    int nchunks;
+    CsrPlan csr;
+    int64_t max_segs;
+    size_t off_delta, off_rowptr, off_col, off_csr, off_segptr, off_segrow, off_segcnt,
+        off_scan_tmp2, off_partial, off_interm, off_dst, off_dqacc, off_dkvacc;
+    size_t bytes;
+};
+
+BwdPlan plan_bwd(const smla_dims& d);
+
+// Scratch of the generic exclusive scan (int32) over n values.
+size_t scan_tmp_bytes(int64_t n);
+
+// ------------------------------------------------------- launch accounting
+// Every launcher calls note_launch() once per kernel it enqueues; the phase
+// profiler attributes the count to the running phase.
+void note_launch(int n = 1);
+
+// ---------------------------------------------------------------- launchers
+// All launchers enqueue on `s` and return cudaGetLastError().
+cudaError_t launch_delta(const uint16_t* o, const uint16_t* dO, float* delta,
+                         int64_t rows, cudaStream_t s);
+cudaError_t launch_dsink(const float* delta, const float* lse, const float* sink,
+                         float* d_sink, int T, int H, cudaStream_t s);
+cudaError_t launch_exclusive_scan(const int32_t* in, int32_t* out, int64_t n,
+                                  void* tmp, cudaStream_t s, bool write_total);
+cudaError_t launch_csr(const int32_t* topk, int T, int topk_w, int r0, int r_len, int num_kv,
+                       int32_t* row_ptr, int32_t* col, char* scratch, const CsrPlan& p,
+                       unsigned* status, cudaStream_t s);
+cudaError_t launch_gather(const int32_t* row_ptr, const int32_t* col, const uint16_t* interm,
+                          int num_kv, int64_t max_segs, int32_t* seg_cnt, int32_t* seg_ptr,
+                          int32_t* seg_row, void* scan_tmp, float* partial, float* dkv_acc,
+                          uint16_t* dkv_out, bool first_chunk, bool last_chunk, cudaStream_t s);
+cudaError_t launch_fwd(const uint16_t* q, const uint16_t* kv, const int32_t* topk,
+                       const float* sink, uint16_t* o, float* lse, int T, int H, int K,
+                       int num_kv, float scale, unsigned* status, cudaStream_t s);
+
+// Per-chunk attention backward core: for ranks [r0, r0+R) of each token, builds
+// interm [T, R, D] bf16 (sum_h P*dO + scale*dS*q) and dsT [T, R, H] bf16
+// (scale * dS, transposed), then accumulates dq.
+struct ChunkArgs {
+    const uint16_t* q; const uint16_t* kv; const uint16_t* dO;
+    const float* lse; const float* delta; const int32_t* topk;
+    int T, H, K, N, r0, R;
+    float scale;
+    uint16_t* interm; uint16_t* dsT;
+    float* dq_acc; uint16_t* dq_out;   // dq_acc NULL when unchunked
+    bool first_chunk, last_chunk;
+    unsigned* status;
+};
+cudaError_t launch_attn_chunk(const ChunkArgs& a, cudaStream_t s);
+
+}  // namespace smla

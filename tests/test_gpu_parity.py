@@ -1,0 +1,205 @@
+"""GPU parity of the CUDA path against the fp64 oracle (small and medium sizes,
+full tensors), plus edge cases, determinism and chunking.
+
+Every call goes through the C ABI (sparse_mla_attention_gb300.api marshals
+torch tensors into libsmla.so).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_mla_attention_gb300 as smla
+from sparse_mla_attention_gb300 import _lib, workloads as W
+from gpu_helpers import Case, compare, custom_inputs, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from sparse_mla_attention_gb300 import build
+    build.build()
+    oracle.build()
+    assert torch.cuda.is_available()
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return Case(W.make_inputs(W.WORKLOADS["tiny"]))
+
+
+@pytest.fixture(scope="module")
+def t1024():
+    return Case(W.make_inputs(W.WORKLOADS["t1024_h64"]))
+
+
+def _run_bwd(c: Case, r_chunk=None, ws=None, out=None):
+    return smla.sparse_mla_bwd(c.q, c.kv, c.do, c.o, c.lse, c.topk, c.sink, scale=c.scale,
+                               r_chunk=r_chunk, workspace=ws, out=out)
+
+
+def _check_full(c: Case, r_chunk=None):
+    dq, dkv, dsink = _run_bwd(c, r_chunk)
+    ref = c.ref_full()
+    compare("dq", to_f64(dq), ref["dq"])
+    compare("dkv", to_f64(dkv), ref["dkv"])
+    if c.sink is not None:
+        compare("d_sink", to_f64(dsink), ref["dsink"])
+    else:
+        assert dsink is None
+
+
+# ------------------------------------------------------------------- CSR
+@pytest.mark.parametrize("name,r0,r_len", [
+    ("tiny", 0, 64), ("tiny", 16, 16), ("t1024_h64", 0, 256), ("t1024_h64", 128, 128),
+    ("headline", 0, 512), ("headline", 384, 128), ("t8192_zipf", 0, 512),
+])
+def test_csr_bit_exact(name, r0, r_len):
+    spec = W.WORKLOADS[name]
+    rng = np.random.Generator(np.random.PCG64(5))
+    topk = W.make_topk(spec, rng)
+    rp, col = smla.csr_build(torch.from_numpy(topk).cuda(), spec.num_kv, r0, r_len)
+    erp, ecol = oracle.csr(topk, spec.num_kv, r0, r_len)
+    assert np.array_equal(rp.cpu().numpy(), erp)
+    assert np.array_equal(col.cpu().numpy(), ecol)
+
+
+def test_csr_edge_cases():
+    rng = np.random.default_rng(0)
+    topk = rng.integers(-1, 7, size=(33, 9)).astype(np.int32)
+    topk[0, :] = 3                          # one row referenced 9 times by one token
+    topk[5, :] = -1
+    for r0, R in ((0, 9), (2, 3), (8, 1)):
+        rp, col = smla.csr_build(torch.from_numpy(topk).cuda(), 7, r0, R)
+        erp, ecol = oracle.csr(topk, 7, r0, R)
+        assert np.array_equal(rp.cpu().numpy(), erp) and np.array_equal(col.cpu().numpy(), ecol)
+    # no valid entry at all, and no token at all
+    rp, col = smla.csr_build(torch.full((4, 5), -1, dtype=torch.int32, device="cuda"), 6)
+    assert rp.cpu().tolist() == [0] * 7 and col.numel() == 0
+    rp, col = smla.csr_build(torch.zeros((0, 5), dtype=torch.int32, device="cuda"), 6)
+    assert rp.cpu().tolist() == [0] * 7
+
+
+# --------------------------------------------------------------- forward
+def test_forward_matches_oracle(tiny):
+    o, lse = smla.sparse_mla_fwd(tiny.q, tiny.kv, tiny.topk, tiny.sink, scale=tiny.scale)
+    _, _, o64, lse64 = oracle.fwd_inputs(tiny.inp)
+    compare("o", to_f64(o), o64, cos_min=0.99999, rel=1e-2)
+    assert np.max(np.abs(to_f64(lse) - lse64)) < 1e-4
+
+
+def test_forward_no_sink_and_masked_rows():
+    c = custom_inputs(1, T=9, H=16, K=40, N=50, sink=False, all_masked_rows=(3,))
+    case = Case(c)
+    o, lse = smla.sparse_mla_fwd(case.q, case.kv, case.topk, None, scale=case.scale)
+    o64, lse64 = oracle.fwd(case.q64, case.kv64, c["topk"], None, case.scale)
+    lse_g = to_f64(lse)
+    assert np.all(np.isneginf(lse_g[3])) and np.all(to_f64(o)[3] == 0)
+    ok = np.isfinite(lse64)
+    assert np.max(np.abs(lse_g[ok] - lse64[ok])) < 1e-4
+    compare("o", to_f64(o), o64, cos_min=0.99999, rel=1e-2)
+
+
+# -------------------------------------------------------------- backward
+def test_bwd_tiny_full(tiny):
+    _check_full(tiny)
+
+
+def test_bwd_t1024_full(t1024):
+    _check_full(t1024)
+
+
+def test_bwd_t1024_chunked_matches_unchunked(t1024):
+    dq1, dkv1, ds1 = _run_bwd(t1024)
+    dq2, dkv2, ds2 = _run_bwd(t1024, r_chunk=64)
+    compare("dq chunked", to_f64(dq2), to_f64(dq1), cos_min=0.99999, rel=1e-2)
+    compare("dkv chunked", to_f64(dkv2), to_f64(dkv1), cos_min=0.99999, rel=1e-2)
+    assert torch.equal(ds1, ds2)
+    ref = t1024.ref_full()
+    compare("dq", to_f64(dq2), ref["dq"])
+    compare("dkv", to_f64(dkv2), ref["dkv"])
+
+
+@pytest.mark.parametrize("H,K,N,T,sink,chunk", [
+    (16, 1, 20, 12, True, 0),       # topk = 1
+    (16, 1, 20, 12, False, 0),
+    (32, 48, 90, 70, True, 16),     # ragged tiles, chunks
+    (64, 200, 260, 130, False, 40), # several rank tiles, no sink, uneven chunk
+    (128, 72, 150, 37, True, 0),
+])
+def test_bwd_custom_shapes(H, K, N, T, sink, chunk):
+    c = Case(custom_inputs(H * 7 + K, T=T, H=H, K=K, N=N, sink=sink,
+                           all_masked_rows=(min(2, T - 1),), r_chunk=chunk))
+    _check_full(c, r_chunk=chunk or None)
+
+
+def test_bwd_empty_T():
+    H, N = 16, 10
+    q = torch.zeros((0, H, 512), dtype=torch.bfloat16, device="cuda")
+    kv = torch.randn((N, 512), device="cuda").bfloat16()
+    topk = torch.zeros((0, 4), dtype=torch.int32, device="cuda")
+    lse = torch.zeros((0, H), dtype=torch.float32, device="cuda")
+    sink = torch.randn(H, device="cuda")
+    dkv0 = torch.full_like(kv, float("nan"))
+    dq, dkv, ds = smla.sparse_mla_bwd(q, kv, q, q, lse, topk, sink,
+                                      out=(torch.empty_like(q), dkv0, torch.full((H,), 7.0, device="cuda")))
+    assert dq.numel() == 0 and torch.all(dkv == 0) and torch.all(ds == 0)
+
+
+def test_bwd_out_of_range_index_reports_and_masks():
+    c = custom_inputs(3, T=8, H=16, K=12, N=20, sink=True, mask_p=0.0)
+    case = Case(c)
+    bad = case.topk.clone()
+    bad[4, 5] = 20          # == num_kv: out of range
+    bad[6, 0] = -7
+    with pytest.raises(_lib.SmlaError) as e:
+        smla.sparse_mla_bwd(case.q, case.kv, case.do, case.o, case.lse, bad, case.sink)
+    assert e.value.code == _lib.SMLA_ERR_INDEX
+    # results equal those with the bad slots masked
+    masked = bad.clone(); masked[4, 5] = -1; masked[6, 0] = -1
+    r1 = smla.sparse_mla_bwd(case.q, case.kv, case.do, case.o, case.lse, bad, case.sink,
+                             check_status=False)
+    r2 = smla.sparse_mla_bwd(case.q, case.kv, case.do, case.o, case.lse, masked, case.sink)
+    torch.cuda.synchronize()
+    for a, b in zip(r1, r2):
+        assert torch.equal(a, b)
+
+
+def test_bwd_nan_poisoned_outputs_and_workspace(t1024):
+    """Every output cell must be written; stale workspace bytes must not leak in."""
+    ws = smla.Workspace()
+    dims = smla.make_dims(t1024.T, t1024.H, t1024.K, t1024.N)
+    buf = ws.get(smla.workspace_size(_lib.SMLA_OP_BWD, dims))
+    buf.fill_(0xFF)
+    dq = torch.full_like(t1024.q, float("nan"))
+    dkv = torch.full_like(t1024.kv, float("nan"))
+    ds = torch.full((t1024.H,), float("nan"), device="cuda")
+    _run_bwd(t1024, ws=ws, out=(dq, dkv, ds))
+    assert torch.isfinite(dq.float()).all() and torch.isfinite(dkv.float()).all()
+    assert torch.isfinite(ds).all()
+    dq2, dkv2, ds2 = _run_bwd(t1024)
+    assert torch.equal(dq, dq2) and torch.equal(dkv, dkv2) and torch.equal(ds, ds2)
+
+
+def test_bwd_bitwise_deterministic(t1024):
+    ws = smla.Workspace()
+    runs = [_run_bwd(t1024, ws=ws) for _ in range(3)] + [_run_bwd(t1024)]
+    for r in runs[1:]:
+        for a, b in zip(runs[0], r):
+            assert torch.equal(a, b)
+    runs = [_run_bwd(t1024, r_chunk=128, ws=ws) for _ in range(2)]
+    for a, b in zip(runs[0], runs[1]):
+        assert torch.equal(a, b)
+
+
+def test_bwd_rejects_bad_input_on_host(t1024):
+    with pytest.raises(TypeError):
+        smla.sparse_mla_bwd(t1024.q.float(), t1024.kv, t1024.do, t1024.o, t1024.lse, t1024.topk)
+    with pytest.raises(ValueError):
+        smla.sparse_mla_bwd(t1024.q, t1024.kv, t1024.do, t1024.o, t1024.lse[:, :3], t1024.topk)
+    with pytest.raises(_lib.SmlaError) as e:
+        smla.sparse_mla_bwd(t1024.q, t1024.kv, t1024.do, t1024.o, t1024.lse, t1024.topk,
+                            t1024.sink, r_chunk=100)
+    assert e.value.code == _lib.SMLA_ERR_RCHUNK
