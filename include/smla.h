@@ -145,6 +145,29 @@ int smla_csr_build(const int32_t* topk, int32_t T, int32_t topk_w, int32_t r0,
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * d_sink without a workspace. The page has no counterpart to this entry point:
+ * it exists for callers that cannot allocate device memory -- because another
+ * allocator (a framework's caching allocator, or an arena reserved at
+ * start-up) owns all of it, or because they run where allocating is not
+ * allowed -- and so cannot hand smla_bwd a workspace. It computes the same
+ * d_sink as smla_bwd, with the same kernels:
+ *   delta[t,h] = sum_d o[t,h,d] * dO[t,h,d];  d_sink[h] = -sum_t exp(sink[h] - lse[t,h]) * delta[t,h]
+ *   dO, o [T,H,D=512] bf16; lse [T,H] fp32; sink [H] fp32 -> d_sink [H] fp32 (all device memory).
+ * The scratch (delta) lives in a 4 MiB array inside the library, so the call
+ * allocates nothing. Limits and rules:
+ *   - T * H must be <= 1048576 (2^20), else SMLA_ERR_SHAPE and nothing runs;
+ *     H must be a multiple of 16 in 16..128.
+ *   - The array exists on every GPU that loads the library, until the process exits.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the array: calls whose kernels overlap on the GPU race,
+ *     so serialize them (one stream, or events between streams).
+ */
+int smla_dsink_static(const uint16_t* dO, const uint16_t* o, const float* lse,
+                      const float* sink, float* d_sink, int32_t T, int32_t H, void* stream);
+
+/*
  * Synchronizes `stream`, then reads the device status word that the last
  * call given this workspace wrote (SMLA_OK, SMLA_ERR_INDEX or
  * SMLA_ERR_TIMEOUT) into *status. Returns SMLA_ERR_CUDA if the stream or

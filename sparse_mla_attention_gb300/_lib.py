@@ -36,7 +36,7 @@ SMLA_OP_FWD, SMLA_OP_BWD, SMLA_OP_CSR = 0, 1, 2
 
 EXPORTED = ("smla_workspace_size", "smla_fwd", "smla_bwd", "smla_csr_build",
             "smla_get_device_status", "smla_status_string", "smla_version",
-            "smla_profiling", "smla_profile_read")
+            "smla_profiling", "smla_profile_read", "smla_dsink_static")
 
 
 class SmlaDims(ctypes.Structure):
@@ -81,6 +81,7 @@ def load(path: str = LIB_PATH):
         lib.smla_bwd.argtypes = [vp] * 10 + [dims_p, vp, sz, vp]
         lib.smla_csr_build.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, sz, vp]
         lib.smla_get_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
+        lib.smla_dsink_static.argtypes = [vp] * 5 + [i32, i32, vp]
         lib.smla_profiling.argtypes = [ctypes.c_int]
         lib.smla_profile_read.argtypes = [ctypes.POINTER(SmlaPhaseStat), ctypes.c_int,
                                           ctypes.POINTER(ctypes.c_int)]
@@ -88,7 +89,7 @@ def load(path: str = LIB_PATH):
         lib.smla_status_string.restype = ctypes.c_char_p
         for name in ("smla_workspace_size", "smla_fwd", "smla_bwd", "smla_csr_build",
                      "smla_get_device_status", "smla_version", "smla_profiling",
-                     "smla_profile_read"):
+                     "smla_profile_read", "smla_dsink_static"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib

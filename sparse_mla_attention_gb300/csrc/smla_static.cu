@@ -1,0 +1,90 @@
+// smla_static.cu -- the allocation-free d_sink entry point.
+//
+// smla_bwd needs a caller-provided workspace, which means the caller must be
+// able to allocate device memory. Some callers cannot: their device memory is
+// wholly owned by another allocator (a framework's caching allocator, or a
+// fixed arena reserved at start-up), or they run where allocation is not
+// allowed at all. For them this file offers d_sink with its one scratch
+// buffer (the per-(t, h) delta = rowsum(O * dO)) held in a file-scope device
+// array instead of a workspace.
+//
+// The array is part of the library image: every GPU on which libsmla.so is
+// loaded holds it (4 MiB) until the process exits. All calls share it, so two
+// calls whose kernels overlap on the GPU race; serialize them (one stream, or
+// events between streams). Every call overwrites the T * H entries it reads,
+// so nothing needs clearing between calls.
+#include <mutex>
+
+#include "smla_internal.cuh"
+
+namespace smla {
+// Largest T * H the static scratch holds: 2^20 fp32 values (4 MiB).
+constexpr int64_t kStaticDeltaMax = int64_t(1) << 20;
+}  // namespace smla
+
+static __device__ __align__(256) float g_static_delta[smla::kStaticDeltaMax];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+float* g_static_delta_addr[kMaxDevices];   // device address of g_static_delta, per device
+
+// In host code `g_static_delta` names a host-side shadow, not device memory;
+// the device address must be looked up once per device, with that device
+// current. Returns nullptr on failure.
+float* static_delta_for(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_static_delta_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_delta) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_static_delta_addr[dev] = static_cast<float*>(p);
+    }
+    return g_static_delta_addr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool disjoint(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return na == 0 || nb == 0 || a0 + na <= b0 || b0 + nb <= a0;
+}
+
+}  // namespace
+
+extern "C" int smla_dsink_static(const uint16_t* dO, const uint16_t* o, const float* lse,
+                                 const float* sink, float* d_sink, int32_t T, int32_t H,
+                                 void* stream) {
+    if (!sink || !d_sink) return SMLA_ERR_NULL;
+    if (T < 0 || H < 16 || H > 128 || H % 16 != 0) return SMLA_ERR_SHAPE;
+    if (int64_t(T) * H > smla::kStaticDeltaMax) return SMLA_ERR_SHAPE;
+    if (T > 0 && (!dO || !o || !lse)) return SMLA_ERR_NULL;
+    const void* ptrs[] = {dO, o, lse, sink, d_sink};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SMLA_ERR_ALIGN;
+    const size_t thd = size_t(T) * H * smla::kD * 2, th4 = size_t(T) * H * 4, h4 = size_t(H) * 4;
+    if (!disjoint(d_sink, h4, dO, thd) || !disjoint(d_sink, h4, o, thd) ||
+        !disjoint(d_sink, h4, lse, th4) || !disjoint(d_sink, h4, sink, h4))
+        return SMLA_ERR_OVERLAP;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SMLA_ERR_CUDA; }
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SMLA_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return SMLA_ERR_ARCH;
+    float* delta = static_delta_for(dev);
+    if (!delta) return SMLA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0)
+        return cudaMemsetAsync(d_sink, 0, h4, s) == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+    if (smla::launch_delta(o, dO, delta, int64_t(T) * H, s) != cudaSuccess) return SMLA_ERR_CUDA;
+    if (smla::launch_dsink(delta, lse, sink, d_sink, T, H, s) != cudaSuccess) return SMLA_ERR_CUDA;
+    return SMLA_OK;
+}
