@@ -199,6 +199,12 @@ def run_ours(args):
 
     spec = W.WORKLOADS[args.workload]
     inp = W.make_inputs(spec)
+    if args.tokens and args.tokens < spec.T:
+        # a token prefix of the workload (profiling runs on small cases)
+        import dataclasses
+        spec = dataclasses.replace(spec, T=args.tokens)
+        for k in ("q", "do", "topk"):
+            inp[k] = np.ascontiguousarray(inp[k][: args.tokens])
     T, H, K, N = spec.T, spec.H, spec.topk, spec.num_kv
 
     def dev_bf16(bits):
@@ -391,6 +397,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="time only the first N tokens of the workload (small profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -18,8 +18,8 @@ namespace smla {
 
 // ------------------------------------------------------------ phase profiler
 namespace prof {
-enum Phase { kDelta, kCsr, kAttn, kGather, kDsink, kFwd, kPhases };
-const char* const kNames[kPhases] = {"delta", "csr", "attn", "gather", "dsink", "fwd"};
+enum Phase { kDelta, kCsr, kSdi, kDq, kGather, kDsink, kFwd, kPhases };
+const char* const kNames[kPhases] = {"delta", "csr", "attn_sdi", "attn_dq", "gather", "dsink", "fwd"};
 std::atomic<long long> g_launches{0};
 bool g_on = false;
 struct Pending { int phase; cudaEvent_t a, b; long long launches; };
@@ -59,11 +59,7 @@ struct Scope {
 
 void note_launch(int n) { prof::g_launches += n; }
 
-cudaError_t launch_attn_chunk_simt(const ChunkArgs& a, cudaStream_t s);
 
-cudaError_t launch_attn_chunk(const ChunkArgs& a, cudaStream_t s) {
-    return launch_attn_chunk_simt(a, s);
-}
 
 BwdPlan plan_bwd(const smla_dims& d) {
     BwdPlan p{};
@@ -85,7 +81,7 @@ BwdPlan plan_bwd(const smla_dims& d) {
     p.off_scan_tmp2 = take(scan_tmp_bytes(p.N));
     p.off_partial = take(size_t(p.max_segs) * kD * 4);
     p.off_interm = take(size_t(nnz_max) * kD * 2);
-    p.off_dst = take(size_t(nnz_max) * size_t(p.H) * 2);
+    p.off_dst = take(size_t(p.T) * round_up_ranks(int(p.R)) * pad_heads(int(p.H)) * 2);
     p.off_dqacc = take(p.nchunks > 1 ? size_t(p.T * p.H) * kD * 4 : 0);
     p.off_dkvacc = take(p.nchunks > 1 ? size_t(p.N) * kD * 4 : 0);
     p.bytes = off;
@@ -291,8 +287,12 @@ int smla_bwd(const uint16_t* q, const uint16_t* kv, const uint16_t* dO, const ui
         a.scale = scale; a.interm = interm; a.dsT = dsT; a.dq_acc = dq_acc; a.dq_out = dq;
         a.first_chunk = first; a.last_chunk = last; a.status = status;
         {
-            prof::Scope ph(prof::kAttn, s);
-            if ((rc = cuda_rc(launch_attn_chunk(a, s)))) return rc;
+            prof::Scope ph(prof::kSdi, s);
+            if ((rc = cuda_rc(launch_attn_sdi(a, s)))) return rc;
+        }
+        {
+            prof::Scope ph(prof::kDq, s);
+            if ((rc = cuda_rc(launch_attn_dq(a, s)))) return rc;
         }
         prof::Scope ph(prof::kGather, s);
         rc = cuda_rc(launch_gather(row_ptr, col, interm, d.num_kv, plan.max_segs,

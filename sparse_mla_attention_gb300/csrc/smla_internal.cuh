@@ -46,6 +46,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // ------------------------------------------------------------ workspace plans
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The scale*dS^T stash of the tensor-core path is [T, Rp, Hp] bf16: ranks padded
+// to whole 128-rank tiles, heads padded to whole 64-column swizzle blocks.
+inline int round_up_ranks(int R) { return (R + 127) / 128 * 128; }
+inline int pad_heads(int H) { return H <= 64 ? 64 : 128; }
+
 // Radix-sort based CSR build parameters.
 constexpr int kRadixBits = 11;
 constexpr int kRadixBuckets = 1 << kRadixBits;   // 2048
@@ -121,6 +126,9 @@ struct ChunkArgs {
     bool first_chunk, last_chunk;
     unsigned* status;
 };
-cudaError_t launch_attn_chunk(const ChunkArgs& a, cudaStream_t s);
+// The two tensor-core kernels of one chunk: S/dP/P/dS + interm (+ dS stash),
+// then dq from the stash. launch_attn_dq must follow launch_attn_sdi.
+cudaError_t launch_attn_sdi(const ChunkArgs& a, cudaStream_t s);
+cudaError_t launch_attn_dq(const ChunkArgs& a, cudaStream_t s);
 
 }  // namespace smla

@@ -2,7 +2,9 @@
 oracle references and the comparison bar.
 
 The bar (for every floating-point output): cosine similarity > 0.999 and
-max |gpu - ref| <= 2e-2 * max |ref|. The CSR is compared bit for bit.
+max |gpu - ref| <= 2e-2 * max |ref|. Where the reference is identically zero
+the bar is an absolute 1e-4 (fp32 rounding of quantities of order 10). The
+CSR is compared bit for bit.
 """
 
 from __future__ import annotations
@@ -15,6 +17,7 @@ from sparse_mla_attention_gb300 import workloads as W
 
 COS_MIN = 0.999
 MAXABS_REL = 2e-2
+ZERO_ATOL = 1e-4
 
 
 def bf16_dev(bits: np.ndarray, device="cuda") -> torch.Tensor:
@@ -39,7 +42,11 @@ def compare(name: str, got: np.ndarray, ref: np.ndarray, cos_min=COS_MIN, rel=MA
     scale = np.max(np.abs(ref)) if ref.size else 0.0
     err = np.max(np.abs(got - ref)) if ref.size else 0.0
     if scale == 0.0:
-        assert err == 0.0, f"{name}: expected exact zeros, max err {err}"
+        # The reference is exactly zero (e.g. dq when topk = 1 and no sink: dS = P (dP - delta)
+        # with dP == delta in exact arithmetic). The GPU forms dP and delta in fp32 with
+        # different summation orders, so it leaves fp32 rounding noise of order
+        # 2^-24 * sum|dO * kv| (about 1e-5 here); bound it absolutely.
+        assert err <= ZERO_ATOL, f"{name}: expected zeros, max err {err}"
         return {"cos": 1.0, "maxabs_rel": 0.0}
     cos = float(got @ ref / (np.linalg.norm(got) * np.linalg.norm(ref) + 1e-300))
     assert cos > cos_min, f"{name}: cos {cos:.6f} <= {cos_min}"
