@@ -9,23 +9,28 @@
 //   dq[t, h, :]    += scale * sum_r dS * kv[idx, :]
 //
 // sdi_kernel (S, dP, P, dS, interm): persistent, one CTA per SM. A work item
-// is (token t, 256 ranks) = two 128-rank tiles. Per tile, one kv tile gathered
-// by TMA (tile::gather4) feeds a single MMA stream that computes S^T and dP^T
-// together: M = 128 ranks, N = 2H (the q rows of token t followed by its dO
-// rows), K = 512, accumulated in TMEM. Epilogue warps turn each TMEM row
-// (one rank) into P and scale*dS, write them back into TMEM as bf16 (the A
-// operand of the next GEMM) and stash scale*dS for the dq kernel. Then
-// interm = [P | scale*dS] x [dO ; q] runs with A from TMEM (M = 128 ranks,
-// N = 64 columns of D per step, K = 2H) and is drained to global memory.
-// TMEM (512 columns): tile g owns columns [256g, 256g+256): S^T | dP^T in
-// [0, 2H), then P^T (bf16 pairs) in [0, H/2) and scale*dS^T in [H/2, H); the
-// interm accumulators double-buffer in [128, 192) and [192, 256).
+// is (token t, 256 ranks) = two 128-rank tiles.
+//  * A stage: per tile, one MMA stream computes S^T and dP^T together:
+//    M = 128 ranks, N = 2H (the q rows of token t followed by its dO rows),
+//    K = 512, in eight 64-column steps. The kv rows of each step are gathered
+//    by two copy warps (16-byte cp.async through L2); the q / dO tiles come
+//    by TMA.
+//  * Epilogue: each TMEM row (one rank) becomes P and scale*dS, written back
+//    into TMEM as bf16 pairs (the A operand of the next GEMM); scale*dS^T is
+//    also stashed in global memory for the dq kernel (staged, TMA store).
+//  * B stage: interm = [P | scale*dS] x [dO ; q] with A from TMEM: M = 128
+//    ranks, N = 128 columns of D per step, K = 2H. Each tile has one
+//    128-column accumulator; the tiles alternate so that one tile's drain
+//    (TMEM -> bf16 -> staging -> TMA store) overlaps the other tile's MMAs.
+// TMEM (512 columns): tile g owns columns [256g, 256g + 256): S^T | dP^T in
+// [0, 2H); then P^T in [0, H/2), scale*dS^T in [H/2, H) and the interm
+// accumulator in [128, 256).
 //
 // dq_kernel: persistent; item = (token, half of D). dq = (scale*dS) x kv:
-// M = 128 (heads, zero-padded), N = 256, K = ranks, both operands MN-major
-// (scale*dS^T rows from the stash, kv rows gathered), accumulated in TMEM
-// (two 256-column buffers) and written as bf16 (or added to an fp32
-// accumulator between rank chunks).
+// M = 128 (heads, zero-padded), N = 256, K = ranks in 64-rank steps, both
+// operands MN-major (scale*dS^T rows by TMA from the stash, kv rows gathered
+// by four copy warps), accumulated in TMEM (two 256-column buffers) and
+// written as bf16 (or added to an fp32 accumulator between rank chunks).
 //
 // Every mbarrier wait is bounded (kWaitNs); a timeout sets SMLA_ERR_TIMEOUT in
 // the status word, stops the CTA's loops, waits (bounded) for its own copies
@@ -42,39 +47,24 @@ namespace {
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
-struct SdiParams {
-    const int32_t* topk;
-    const float* lse;
-    const float* delta;
-    uint16_t* interm;     // [T, R, 512]
-    uint16_t* dsT;        // [T, Rp, Hp]
-    int T, K, N, r0, R, Rp, Hp;
-    int npairs;           // items per token: ceil(R / 256)
-    int tiles_last;       // tiles (1 or 2) in a token's last item
-    float scale;
-    unsigned* status;
-};
-
-struct SdiShared {
-    uint64_t full[8], empty[8];
-    uint64_t s_full, p_ready, x_full[2], x_empty[2], b_done[2], drain;
-    uint32_t tbase;
-    volatile int abort_flag;
-    int idx[256];
-};
-
-template <int H>
-struct SdiCfg {
-    static constexpr int kQBytes = H * 128;                 // H rows x 64 columns bf16
-    static constexpr int kKvBytes = 128 * 128;              // 128 ranks x 64 columns bf16
-    static constexpr int kSlotBytes = 2 * kQBytes + 2 * kKvBytes;
-    static constexpr int kSlotsRaw = 196608 / kSlotBytes;
-    static constexpr int kSlots = kSlotsRaw > 8 ? 8 : kSlotsRaw;
-    static constexpr int kThreads = 320;                    // TMA, MMA, 8 epilogue warps
-    static constexpr int kSmem = int(sizeof(SdiShared)) + 1024 + kSlots * kSlotBytes;
-    static constexpr uint32_t kIdescA = idesc_bf16(128, 2 * H, false, false);
-    static constexpr uint32_t kIdescB = idesc_bf16(128, 64, false, true);
-};
+// Optional phase timestamps (compiled only with -DSMLA_TRACE; the library
+// build leaves them out): per kernel, CTA (< 8) and item (< 8), 64 events.
+constexpr int kTraceCtas = 8, kTraceItems = 8, kTraceEvents = 64;
+}  // namespace
+#ifdef SMLA_TRACE
+__device__ unsigned long long g_smla_trace[2 * kTraceCtas * kTraceItems * kTraceEvents];
+#define SMLA_TRACE_EV(kid, it, ev)                                                          \
+    do {                                                                                    \
+        if (blockIdx.x < kTraceCtas && (it) < kTraceItems)                                  \
+            g_smla_trace[(((kid) * kTraceCtas + blockIdx.x) * kTraceItems + (it)) *         \
+                             kTraceEvents + (ev)] = globaltimer_ns();                       \
+    } while (0)
+#else
+#define SMLA_TRACE_EV(kid, it, ev) \
+    do {                           \
+    } while (0)
+#endif
+namespace {
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -89,10 +79,64 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
     return false;
 }
 
+__device__ __forceinline__ void advance(int& slot, uint32_t& phase, int nslots) {
+    if (++slot == nslots) { slot = 0; phase ^= 1u; }
+}
+
+// Packs 8 fp32 values into one 16-byte piece of bf16.
+__device__ __forceinline__ uint4 pack8(const uint32_t* v) {
+    return make_uint4(pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                      pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                      pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                      pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
+}
+
+// ====================================================================== SDI
+struct SdiParams {
+    const uint16_t* kv;   // [N, 512]
+    const int32_t* topk;
+    const float* lse;
+    const float* delta;
+    uint16_t* interm;     // [T, R, 512]
+    int T, K, N, r0, R, Rp, Hp;
+    int npairs;           // items per token: ceil(R / 256)
+    int tiles_last;       // tiles (1 or 2) in a token's last item
+    float scale;
+    unsigned* status;
+};
+
+struct SdiShared {
+    uint64_t full[8], empty[8];
+    uint64_t s_full, p_ready, x_full[2], x_empty[2], b_done[2], drain;
+    uint32_t tbase;
+    volatile int abort_flag;
+};
+
+// Per epilogue warp: a 32-row x 128-byte staging tile that turns one-row-per-
+// lane TMEM data into one TMA store; 16-byte pieces are placed with the
+// 128-byte swizzle the store's tensor map uses (which also spreads banks).
+constexpr int kStageBytes = 32 * 128;
+
 template <int H>
-__global__ void __launch_bounds__(320, 1)
+struct SdiCfg {
+    static constexpr int kQBytes = H * 128;                 // H rows x 64 columns bf16
+    static constexpr int kKvBytes = 128 * 128;              // 128 ranks x 64 columns bf16
+    static constexpr int kSlotBytes = 2 * kQBytes + 2 * kKvBytes;
+    static constexpr int kSlotsRaw = 196608 / kSlotBytes;
+    static constexpr int kSlots = kSlotsRaw > 8 ? 8 : kSlotsRaw;
+    static constexpr int kThreads = 384;    // TMA, MMA, 8 epilogue warps, 2 copy warps
+    static constexpr int kSmem = int(sizeof(SdiShared)) + 1024 + kSlots * kSlotBytes + 8 * kStageBytes;
+    static constexpr uint32_t kIdescA = idesc_bf16(128, 2 * H, false, false);
+    static constexpr uint32_t kIdescB = idesc_bf16(128, 128, false, true);
+    static constexpr int kUses = 12;        // ring uses per item: 8 A-stage + 4 B-stage
+    static_assert(kSlots >= 3, "the copy pipeline needs at least three slots");
+};
+
+template <int H>
+__global__ void __launch_bounds__(384, 1)
 sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
-           const __grid_constant__ CUtensorMap map_kv, const SdiParams p) {
+           const __grid_constant__ CUtensorMap map_im, const __grid_constant__ CUtensorMap map_ds,
+           const SdiParams p) {
     using C = SdiCfg<H>;
     extern __shared__ uint8_t smem_raw[];
     SdiShared& sh = *reinterpret_cast<SdiShared*>(smem_raw);
@@ -101,13 +145,14 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     const int nitems = p.T * p.npairs;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kSlots; ++s) { mbar_init(&sh.full[s], 1); mbar_init(&sh.empty[s], 1); }
+        // full: the TMA thread's arrive (with the q / dO bytes) + 64 copy threads
+        for (int s = 0; s < C::kSlots; ++s) { mbar_init(&sh.full[s], 65); mbar_init(&sh.empty[s], 1); }
         mbar_init(&sh.s_full, 1);
         mbar_init(&sh.p_ready, 8);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&sh.x_full[b], 1);
-            mbar_init(&sh.x_empty[b], 8);
-            mbar_init(&sh.b_done[b], 1);
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(&sh.x_full[g], 1);   // tile g's interm accumulator is ready
+            mbar_init(&sh.x_empty[g], 4);  // tile g's 4 epilogue warps have read it
+            mbar_init(&sh.b_done[g], 1);
         }
         mbar_init(&sh.drain, 1);
         sh.abort_flag = 0;
@@ -120,84 +165,148 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     const uint32_t tbase = sh.tbase;
 
     if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
+        // ----------------------------------------------- TMA producer (q, dO)
+        if (lane == 0) {
+            int slot = 0; uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            int it = 0;
+            for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
+                SMLA_TRACE_EV(0, it, 0);
+                const int t = item / p.npairs;
+                for (int c = 0; c < C::kUses; ++c) {
+                    ok = wait_or_abort(&sh.empty[slot], phase ^ 1u, &sh.abort_flag, p.status);
+                    if (!ok) break;
+                    uint8_t* sb = slots + slot * C::kSlotBytes;
+                    SMLA_TRACE_EV(0, it, 48 + c);
+                    if (c < 8) {
+                        // A stage: q and dO columns [64c, 64c + 64)
+                        mbar_arrive_expect_tx(&sh.full[slot], 2 * C::kQBytes);
+                        tma_load_2d(sb, &map_q, c * 64, t * H, &sh.full[slot]);
+                        tma_load_2d(sb + C::kQBytes, &map_do, c * 64, t * H, &sh.full[slot]);
+                    } else {
+                        // B stage: q and dO columns [128b, 128b + 128), two 64-column
+                        // blocks each; the copy warps skip these uses, so arrive for them.
+                        const int b = c - 8;
+                        mbar_arrive_expect_tx(&sh.full[slot], 4 * C::kQBytes);
+                        tma_load_2d(sb, &map_q, b * 128, t * H, &sh.full[slot]);
+                        tma_load_2d(sb + C::kQBytes, &map_q, b * 128 + 64, t * H, &sh.full[slot]);
+                        tma_load_2d(sb + 2 * C::kQBytes, &map_do, b * 128, t * H, &sh.full[slot]);
+                        tma_load_2d(sb + 3 * C::kQBytes, &map_do, b * 128 + 64, t * H, &sh.full[slot]);
+                        mbar_arrive_cnt(&sh.full[slot], 64);
+                    }
+                    ++issued;
+                    advance(slot, phase, C::kSlots);
+                }
+            }
+            if (sh.abort_flag) {
+                // bounded wait for this thread's own copies still in flight
+                int s = slot; uint32_t ph = phase;
+                for (int k = 0; k < C::kSlots && k < issued; ++k) {
+                    if (--s < 0) { s = C::kSlots - 1; ph ^= 1u; }
+                    mbar_wait(&sh.full[s], ph, kWaitNs / 8);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 10) {
+        // ------------------------------------------------ kv gather (cp.async)
+        // In round i (0..31) copy warp gw copies rows 8i + 4gw .. +3 of the
+        // item's 256 ranks; lane l copies the 16-byte piece (l & 7) of row
+        // (l >> 3) into the 128-byte-swizzled tile. Lane l keeps the 32 row
+        // indices it needs in registers, loaded one item ahead.
+        const int gw = warp - 10;
         int slot = 0; uint32_t phase = 0;
-        int issued = 0;   // slot fills whose completion this warp has not seen
         bool ok = true;
-        for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
+        int idx_cur[32], idx_nxt[32];
+        auto load_idx = [&](int item, int (&out)[32]) {
             const int t = item / p.npairs, pr = item - t * p.npairs;
-            const int ntiles = pr == p.npairs - 1 ? p.tiles_last : 2;
-            const int rl0 = pr * 256;
-            for (int i = lane; i < 256; i += 32) {
-                const int rl = rl0 + i;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int rl = pr * 256 + 8 * i + 4 * gw + (lane >> 3);
                 int j = 0;
                 if (rl < p.R) {
                     j = __ldg(p.topk + int64_t(t) * p.K + p.r0 + rl);
                     if (j < -1 || j >= p.N) { flag_status(p.status, SMLA_ERR_INDEX); j = 0; }
-                    if (j < 0) j = 0;            // masked: any real row; its P is zeroed
+                    if (j < 0) j = 0;              // masked: any real row; its P is zeroed
                 }
-                sh.idx[i] = j;
+                out[i] = j;
             }
-            __syncwarp();
-            if (lane == 0) {
-                for (int c = 0; c < 16 && ok; ++c) {
-                    ok = wait_or_abort(&sh.empty[slot], phase ^ 1u, &sh.abort_flag, p.status);
-                    if (!ok) break;
-                    uint8_t* sb = slots + slot * C::kSlotBytes;
-                    const int dc = c & 7;
-                    const bool a_stage = c < 8;
-                    const uint32_t bytes = 2 * C::kQBytes + (a_stage ? ntiles * C::kKvBytes : 0);
-                    mbar_arrive_expect_tx(&sh.full[slot], bytes);
-                    tma_load_2d(sb, &map_q, dc * 64, t * H, &sh.full[slot]);
-                    tma_load_2d(sb + C::kQBytes, &map_do, dc * 64, t * H, &sh.full[slot]);
-                    if (a_stage) {
-                        for (int g = 0; g < ntiles; ++g) {
-                            uint8_t* kvb = sb + 2 * C::kQBytes + g * C::kKvBytes;
-                            const int* ix = sh.idx + g * 128;
-                            for (int q4 = 0; q4 < 32; ++q4)
-                                tma_gather4(kvb + q4 * 512, &map_kv, dc * 64, ix[4 * q4],
-                                            ix[4 * q4 + 1], ix[4 * q4 + 2], ix[4 * q4 + 3],
-                                            &sh.full[slot]);
-                        }
+        };
+        if (int(blockIdx.x) < nitems) load_idx(blockIdx.x, idx_cur);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) idx_nxt[i] = 0;
+        const char* kvbase = reinterpret_cast<const char*>(p.kv) + (lane & 7) * 16;
+        // Slots whose copies are issued but not yet signalled. At most kSlots - 2
+        // stay pending, so the next slot to fill never waits for one of them.
+        int pend[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        int npend = 0;
+        auto flush_one = [&]() {
+            fence_proxy_async_smem();
+            mbar_arrive(&sh.full[pend[0]]);
+#pragma unroll
+            for (int k = 0; k + 1 < 8; ++k) pend[k] = pend[k + 1];
+            --npend;
+        };
+        for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
+            const int pr = item % p.npairs;
+            const int ntiles = pr == p.npairs - 1 ? p.tiles_last : 2;
+            for (int c = 0; c < 8; ++c) {
+                if (lane == 0) ok = wait_or_abort(&sh.empty[slot], phase ^ 1u, &sh.abort_flag, p.status);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                uint8_t* kvb = slots + slot * C::kSlotBytes + 2 * C::kQBytes;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int row = 8 * i + 4 * gw + (lane >> 3);   // 0..255 (tile = row >> 7)
+                    if ((row >> 7) < ntiles) {
+                        const int rr = row & 127;
+                        cp_async16(kvb + (row >> 7) * C::kKvBytes + rr * 128 + (((lane & 7) ^ (rr & 7)) << 4),
+                                   kvbase + int64_t(idx_cur[i]) * (kD * 2) + c * 128);
                     }
-                    ++issued;
-                    if (++slot == C::kSlots) { slot = 0; phase ^= 1u; }
                 }
+                cp_async_commit();
+                pend[npend++] = slot;
+                if (npend == C::kSlots - 1) { cp_async_wait<C::kSlots - 2>(); flush_one(); }
+                if (c == 7) {
+                    // signal what is left, then load the next item's indices
+                    cp_async_wait<0>();
+                    while (npend > 0) flush_one();
+                    const int next = item + gridDim.x;
+                    if (next < nitems) load_idx(next, idx_nxt);
+                }
+                advance(slot, phase, C::kSlots);
             }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            __syncwarp();
+            // the B-stage uses of the ring are signalled by the TMA thread
+            for (int k = 8; k < C::kUses; ++k) advance(slot, phase, C::kSlots);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) idx_cur[i] = idx_nxt[i];
         }
-        if (lane == 0 && sh.abort_flag) {
-            // bounded wait for this warp's own copies still in flight
-            int s = slot; uint32_t ph = phase;
-            for (int k = 0; k < C::kSlots && k < issued; ++k) {
-                if (--s < 0) { s = C::kSlots - 1; ph ^= 1u; }
-                mbar_wait(&sh.full[s], ph, kWaitNs / 8);
-            }
-        }
+        cp_async_wait<0>();
     } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
+        // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             int slot = 0; uint32_t phase = 0;
-            uint32_t xe_done[2] = {0, 0};
+            uint32_t xe_done[2] = {0, 0};   // drains of tile g's accumulator seen
+            uint32_t x_uses[2] = {0, 0};    // accumulations of tile g issued
             bool ok = true;
             int it = 0;
             for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
-                const int t = item / p.npairs, pr = item - t * p.npairs;
-                (void)t;
+                const int pr = item % p.npairs;
                 const int ntiles = pr == p.npairs - 1 ? p.tiles_last : 2;
-                // A stage: S^T | dP^T for each tile.
+                // A stage may overwrite TMEM only after the previous item's B stage
+                // read P / dS, and (when S^T | dP^T reach column 128) after its drains.
                 if (it > 0) {
                     ok = ok && wait_or_abort(&sh.b_done[0], (it - 1) & 1, &sh.abort_flag, p.status);
                     ok = ok && wait_or_abort(&sh.b_done[1], (it - 1) & 1, &sh.abort_flag, p.status);
-                    if (2 * H > 128) {   // S^T | dP^T overlaps the interm buffers: wait for the drains
-                        for (int b = 0; b < 2 && ok; ++b)
-                            while (ok && xe_done[b] < uint32_t(it) * 4u) {
-                                ok = wait_or_abort(&sh.x_empty[b], xe_done[b] & 1u, &sh.abort_flag, p.status);
-                                ++xe_done[b];
+                    if (2 * H > 128)
+                        for (int g = 0; g < 2 && ok; ++g)
+                            while (ok && xe_done[g] < x_uses[g]) {
+                                ok = wait_or_abort(&sh.x_empty[g], xe_done[g] & 1u, &sh.abort_flag, p.status);
+                                ++xe_done[g];
                             }
-                    }
                 }
+                SMLA_TRACE_EV(0, it, 3);
                 for (int c = 0; c < 8 && ok; ++c) {
                     ok = wait_or_abort(&sh.full[slot], phase, &sh.abort_flag, p.status);
                     if (!ok) break;
@@ -205,64 +314,73 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     const uint32_t sb = smem_u32(slots + slot * C::kSlotBytes);
                     for (int g = 0; g < ntiles; ++g) {
                         const uint32_t kvb = sb + 2 * C::kQBytes + g * C::kKvBytes;
-                        for (int k = 0; k < 4; ++k) {
-                            const uint64_t ad = sdesc_sw128(kvb + k * 32, 16, 1024);
-                            const uint64_t bd = sdesc_sw128(sb + k * 32, 16, 1024);
-                            mma_ss(tbase + g * 256, ad, bd, C::kIdescA, (c | k) != 0);
-                        }
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_ss(tbase + g * 256, sdesc_sw128(kvb + k * 32, 16, 1024),
+                                   sdesc_sw128(sb + k * 32, 16, 1024), C::kIdescA, (c | k) != 0);
                     }
                     mma_commit(&sh.empty[slot]);
-                    if (++slot == C::kSlots) { slot = 0; phase ^= 1u; }
+                    advance(slot, phase, C::kSlots);
                 }
                 if (!ok) break;
                 mma_commit(&sh.s_full);
+                SMLA_TRACE_EV(0, it, 4);
                 ok = wait_or_abort(&sh.p_ready, it & 1, &sh.abort_flag, p.status);
                 if (!ok) break;
+                SMLA_TRACE_EV(0, it, 5);
                 tc_fence_after();
-                // B stage: interm columns [64 dc, 64 dc + 64) for each tile.
-                for (int c = 0; c < 8 && ok; ++c) {
+                // B stage: interm columns [128c, 128c + 128), tiles alternating.
+                for (int c = 0; c < 4 && ok; ++c) {
                     ok = wait_or_abort(&sh.full[slot], phase, &sh.abort_flag, p.status);
-                    const int b = c & 1;
-                    const uint32_t need = uint32_t(it) * 4u + uint32_t(c >> 1);
-                    while (ok && xe_done[b] < need) {
-                        ok = wait_or_abort(&sh.x_empty[b], xe_done[b] & 1u, &sh.abort_flag, p.status);
-                        ++xe_done[b];
-                    }
+                    SMLA_TRACE_EV(0, it, 16 + c);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t sb = smem_u32(slots + slot * C::kSlotBytes);
-                    for (int g = 0; g < ntiles; ++g) {
+                    for (int g = 0; g < ntiles && ok; ++g) {
+                        while (ok && xe_done[g] < x_uses[g]) {
+                            ok = wait_or_abort(&sh.x_empty[g], xe_done[g] & 1u, &sh.abort_flag, p.status);
+                            ++xe_done[g];
+                        }
+                        if (!ok) break;
+                        tc_fence_after();
+                        SMLA_TRACE_EV(0, it, 24 + 2 * c + g);
                         const uint32_t tile = tbase + g * 256;
 #pragma unroll
                         for (int ks = 0; ks < 2 * H / 16; ++ks) {
                             const bool pterm = ks < H / 16;
                             const int kk = pterm ? ks : ks - H / 16;
                             const uint32_t acol = pterm ? kk * 8 : H / 2 + kk * 8;
-                            const uint32_t bt = (pterm ? sb + C::kQBytes : sb) + kk * 2048;
-                            mma_ts(tile + 128 + 64 * b, tile + acol, sdesc_sw128(bt, 8192, 1024),
+                            // dO (P term) or q (dS term): two 64-column blocks of H rows
+                            const uint32_t bt = (pterm ? sb + 2 * C::kQBytes : sb) + kk * 2048;
+                            mma_ts(tile + 128, tile + acol, sdesc_sw128(bt, C::kQBytes, 1024),
                                    C::kIdescB, ks != 0);
                         }
+                        mma_commit(&sh.x_full[g]);
+                        ++x_uses[g];
                     }
                     mma_commit(&sh.empty[slot]);
-                    mma_commit(&sh.x_full[b]);
-                    if (++slot == C::kSlots) { slot = 0; phase ^= 1u; }
+                    advance(slot, phase, C::kSlots);
                 }
                 if (!ok) break;
                 mma_commit(&sh.b_done[0]);
                 mma_commit(&sh.b_done[1]);
+                SMLA_TRACE_EV(0, it, 6);
             }
-            // all MMAs issued by this thread finish before TMEM is freed
+            // every MMA issued by this thread completes before TMEM is freed
             mma_commit(&sh.drain);
             mbar_wait(&sh.drain, 0, kWaitNs);
         }
         __syncwarp();
     } else {
-        // --------------------------------------------------------- epilogue
+        // ----------------------------------------------------------- epilogue
         const int g = (warp - 2) >> 2;                  // tile of this warp group
         const int quarter = warp & 3;                   // TMEM lane quarter of this warp
         const int r = quarter * 32 + lane;              // TMEM lane = rank inside the tile
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+        uint8_t* stage = slots + C::kSlots * C::kSlotBytes + (warp - 2) * kStageBytes;
         const float c1 = p.scale * kLog2e;
+        constexpr int kHw = (H + 31) / 32;              // head words per lane
+        uint32_t x_use = 0;                             // accumulations of this tile consumed
         int it = 0;
         for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++it) {
             if (sh.abort_flag) break;
@@ -270,93 +388,145 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             const int ntiles = pr == p.npairs - 1 ? p.tiles_last : 2;
             const bool active = g < ntiles;
             const int rl = pr * 256 + g * 128 + r;
-            const float* lse_t = p.lse + int64_t(t) * H;
-            const float* delta_t = p.delta + int64_t(t) * H;
+            const int row0 = pr * 256 + g * 128 + quarter * 32;   // first rank of this warp
+            // lane l holds lse * log2(e) and delta of heads l, l + 32, ...
+            float lse_w[kHw], del_w[kHw];
+#pragma unroll
+            for (int k = 0; k < kHw; ++k) {
+                const int h = k * 32 + lane;
+                lse_w[k] = h < H ? __ldg(p.lse + int64_t(t) * H + h) * kLog2e : 0.f;
+                del_w[k] = h < H ? __ldg(p.delta + int64_t(t) * H + h) : 0.f;
+            }
+            bool valid = false;
+            if (active && rl < p.R) {
+                const int j = __ldg(p.topk + int64_t(t) * p.K + p.r0 + rl);
+                valid = j >= 0 && j < p.N;
+            }
             if (!wait_or_abort(&sh.s_full, it & 1, &sh.abort_flag, p.status)) break;
+            if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 7);
             tc_fence_after();
             if (active) {
-                bool valid = false;
-                if (rl < p.R) {
-                    const int j = __ldg(p.topk + int64_t(t) * p.K + p.r0 + rl);
-                    valid = j >= 0 && j < p.N;
-                }
                 const uint32_t trow = tbase + lane_off + g * 256;
                 uint32_t dsp[H / 2];
 #pragma unroll
-                for (int c16 = 0; c16 < H / 16; ++c16) {
-                    uint32_t sv[16], dv[16];
-                    tmem_ld16(trow + c16 * 16, sv);
-                    tmem_ld16(trow + H + c16 * 16, dv);
-                    tmem_wait_ld();
-                    uint32_t pp[8];
+                for (int c16 = 0; c16 < H / 16; c16 += 2) {
+                    const int nch = (c16 + 1 < H / 16) ? 2 : 1;
+                    uint32_t sv[2][16], dv[2][16];
 #pragma unroll
-                    for (int j2 = 0; j2 < 8; ++j2) {
-                        float pv[2], dsv[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int h = c16 * 16 + 2 * j2 + u;
-                            const float s = __uint_as_float(sv[2 * j2 + u]);
-                            const float dp = __uint_as_float(dv[2 * j2 + u]);
-                            const float pe = valid ? exp2f(fmaf(s, c1, -__ldg(lse_t + h) * kLog2e)) : 0.f;
-                            pv[u] = pe;
-                            dsv[u] = valid ? p.scale * pe * (dp - __ldg(delta_t + h)) : 0.f;
+                    for (int u = 0; u < 2; ++u)
+                        if (u < nch) {
+                            tmem_ld16(trow + (c16 + u) * 16, sv[u]);
+                            tmem_ld16(trow + H + (c16 + u) * 16, dv[u]);
                         }
-                        pp[j2] = pack_bf16x2(pv[0], pv[1]);
-                        dsp[c16 * 8 + j2] = pack_bf16x2(dsv[0], dsv[1]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        if (u >= nch) break;
+                        uint32_t pp[8];
+#pragma unroll
+                        for (int j2 = 0; j2 < 8; ++j2) {
+                            float pv[2], dsv[2];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int h = (c16 + u) * 16 + 2 * j2 + e;
+                                const float l2 = __shfl_sync(0xffffffffu, lse_w[h >> 5], h & 31);
+                                const float de = __shfl_sync(0xffffffffu, del_w[h >> 5], h & 31);
+                                const float s = __uint_as_float(sv[u][2 * j2 + e]);
+                                const float dp = __uint_as_float(dv[u][2 * j2 + e]);
+                                const float pe = valid ? exp2f(fmaf(s, c1, -l2)) : 0.f;
+                                pv[e] = pe;
+                                dsv[e] = valid ? p.scale * pe * (dp - de) : 0.f;
+                            }
+                            pp[j2] = pack_bf16x2(pv[0], pv[1]);
+                            dsp[(c16 + u) * 8 + j2] = pack_bf16x2(dsv[0], dsv[1]);
+                        }
+                        // P^T over S^T columns already read
+                        tmem_st8(trow + (c16 + u) * 8, pp);
                     }
-                    tmem_st8(trow + c16 * 8, pp);
                 }
 #pragma unroll
                 for (int c16 = 0; c16 < H / 16; ++c16) tmem_st8(trow + H / 2 + c16 * 8, dsp + c16 * 8);
                 tmem_wait_st();
-                // stash scale * dS^T for the dq kernel (rows up to the padded rank count)
-                uint4* dst = reinterpret_cast<uint4*>(p.dsT + (int64_t(t) * p.Rp + rl) * p.Hp);
+                // stash scale * dS^T for the dq kernel: per 64-head block the warp's 32
+                // rows go through the staging tile and one TMA store (heads >= H are 0)
 #pragma unroll
-                for (int v = 0; v < H / 8; ++v)
-                    dst[v] = make_uint4(dsp[4 * v], dsp[4 * v + 1], dsp[4 * v + 2], dsp[4 * v + 3]);
-                for (int v = H / 8; v < p.Hp / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+                for (int hb = 0; hb < (H + 63) / 64; ++hb) {
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                    uint4* srow = reinterpret_cast<uint4*>(stage + lane * 128);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        const int w0 = hb * 32 + 4 * v;
+                        srow[v ^ (lane & 7)] = w0 < H / 2
+                            ? make_uint4(dsp[w0], dsp[w0 + 1], dsp[w0 + 2], dsp[w0 + 3])
+                            : make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&map_ds, hb * 64, t * p.Rp + row0, stage);
+                        bulk_commit();
+                    }
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.p_ready);
-            // drain interm columns 64 dc .. 64 dc + 63
+            if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 8);
+            // drain interm columns [128c, 128c + 128) of this warp's tile, in halves
             bool ok = true;
-            for (int c = 0; c < 8; ++c) {
-                const int b = c & 1;
-                const uint32_t use = uint32_t(it) * 4u + uint32_t(c >> 1);
-                if (!wait_or_abort(&sh.x_full[b], use & 1u, &sh.abort_flag, p.status)) { ok = false; break; }
+            for (int c = 0; c < 4 && active; ++c) {
+                if (!wait_or_abort(&sh.x_full[g], x_use & 1u, &sh.abort_flag, p.status)) { ok = false; break; }
+                ++x_use;
+                if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 32 + c);
                 tc_fence_after();
-                if (active) {
-                    const uint32_t xa = tbase + lane_off + g * 256 + 128 + 64 * b;
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint32_t xa = tbase + lane_off + g * 256 + 128 + 64 * hh;
                     uint32_t v0[32], v1[32];
                     tmem_ld32(xa, v0);
                     tmem_ld32(xa + 32, v1);
                     tmem_wait_ld();
-                    if (rl < p.R) {
-                        uint4* out = reinterpret_cast<uint4*>(
-                            p.interm + (int64_t(t) * p.R + rl) * kD + 64 * c);
+                    if (hh == 1) {   // the accumulator is read: the MMA may reuse it
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sh.x_empty[g]);
+                    }
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                    uint4* srow = reinterpret_cast<uint4*>(stage + lane * 128);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            out[v] = make_uint4(
-                                pack_bf16x2(__uint_as_float(v0[8 * v]), __uint_as_float(v0[8 * v + 1])),
-                                pack_bf16x2(__uint_as_float(v0[8 * v + 2]), __uint_as_float(v0[8 * v + 3])),
-                                pack_bf16x2(__uint_as_float(v0[8 * v + 4]), __uint_as_float(v0[8 * v + 5])),
-                                pack_bf16x2(__uint_as_float(v0[8 * v + 6]), __uint_as_float(v0[8 * v + 7])));
+                    for (int v = 0; v < 4; ++v) srow[v ^ (lane & 7)] = pack8(v0 + 8 * v);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            out[4 + v] = make_uint4(
-                                pack_bf16x2(__uint_as_float(v1[8 * v]), __uint_as_float(v1[8 * v + 1])),
-                                pack_bf16x2(__uint_as_float(v1[8 * v + 2]), __uint_as_float(v1[8 * v + 3])),
-                                pack_bf16x2(__uint_as_float(v1[8 * v + 4]), __uint_as_float(v1[8 * v + 5])),
-                                pack_bf16x2(__uint_as_float(v1[8 * v + 6]), __uint_as_float(v1[8 * v + 7])));
+                    for (int v = 0; v < 4; ++v) srow[(v + 4) ^ (lane & 7)] = pack8(v1 + 8 * v);
+                    const int col = 128 * c + 64 * hh;
+                    if (row0 + 32 <= p.R) {
+                        // the warp's 32 ranks all belong to this token: one TMA store
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&map_im, col, t * p.R + row0, stage);
+                            bulk_commit();
+                        }
+                    } else {
+                        // ragged last rows of a token: plain stores of the rows < R
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int rr = 4 * k + (lane >> 3), piece = lane & 7;
+                            const uint4 val = reinterpret_cast<const uint4*>(stage + rr * 128)[piece ^ (rr & 7)];
+                            if (row0 + rr < p.R)
+                                reinterpret_cast<uint4*>(p.interm + (int64_t(t) * p.R + row0 + rr) * kD + col)[piece] = val;
+                        }
+                        __syncwarp();
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.x_empty[b]);
+                if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 40 + c);
             }
+            if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 9);
             if (!ok) break;
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -366,8 +536,9 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     }
 }
 
-// ------------------------------------------------------------------- dq
+// ======================================================================= dq
 struct DqParams {
+    const uint16_t* kv;   // [N, 512]
     const int32_t* topk;
     float* dq_acc;        // fp32 [T, H, 512] between chunks, or nullptr
     uint16_t* dq_out;     // bf16 [T, H, 512]
@@ -381,7 +552,6 @@ struct DqShared {
     uint64_t d_full[2], d_empty[2], drain;
     uint32_t tbase;
     volatile int abort_flag;
-    int idx[64];
 };
 
 constexpr int kDqSlots = 4;
@@ -392,9 +562,8 @@ constexpr int kDqSmem = int(sizeof(DqShared)) + 1024 + kDqSlots * kDqSlotBytes;
 constexpr uint32_t kDqIdesc = idesc_bf16(128, 256, true, true);
 
 template <int H>
-__global__ void __launch_bounds__(192, 1)
-dq_kernel(const __grid_constant__ CUtensorMap map_ds, const __grid_constant__ CUtensorMap map_kv,
-          const DqParams p) {
+__global__ void __launch_bounds__(320, 1)
+dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
     extern __shared__ uint8_t smem_raw[];
     DqShared& sh = *reinterpret_cast<DqShared*>(smem_raw);
     uint8_t* slots = align1024(smem_raw + sizeof(DqShared));
@@ -403,7 +572,8 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const __grid_constant__ CU
     const int nkc = p.Rp / 64;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kDqSlots; ++s) { mbar_init(&sh.full[s], 1); mbar_init(&sh.empty[s], 1); }
+        // full: the TMA thread's arrive (with the dS bytes) + 128 copy threads
+        for (int s = 0; s < kDqSlots; ++s) { mbar_init(&sh.full[s], 129); mbar_init(&sh.empty[s], 1); }
         for (int b = 0; b < 2; ++b) { mbar_init(&sh.d_full[b], 1); mbar_init(&sh.d_empty[b], 4); }
         mbar_init(&sh.drain, 1);
         sh.abort_flag = 0;
@@ -416,50 +586,96 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const __grid_constant__ CU
     const uint32_t tbase = sh.tbase;
 
     if (warp == 0) {
-        int slot = 0; uint32_t phase = 0; int issued = 0;
-        bool ok = true;
-        for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
-            const int t = item >> 1, half = item & 1;
-            for (int kc = 0; kc < nkc && ok; ++kc) {
-                for (int i = lane; i < 64; i += 32) {
-                    const int rl = kc * 64 + i;
-                    int j = 0;
-                    if (rl < p.R) {
-                        j = __ldg(p.topk + int64_t(t) * p.K + p.r0 + rl);
-                        if (j < 0 || j >= p.N) j = 0;     // masked or invalid: its dS is zero
-                    }
-                    sh.idx[i] = j;
-                }
-                __syncwarp();
-                if (lane == 0) {
+        // -------------------------------------- TMA producer (scale*dS^T tiles)
+        if (lane == 0) {
+            int slot = 0; uint32_t phase = 0; int issued = 0;
+            bool ok = true;
+            int it = 0;
+            for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
+                const int t = item >> 1;
+                SMLA_TRACE_EV(1, it, 0);
+                for (int kc = 0; kc < nkc; ++kc) {
                     ok = wait_or_abort(&sh.empty[slot], phase ^ 1u, &sh.abort_flag, p.status);
-                }
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                if (ok && lane == 0) {
+                    if (!ok) break;
                     uint8_t* sb = slots + slot * kDqSlotBytes;
-                    mbar_arrive_expect_tx(&sh.full[slot], kDqSlotBytes);
+                    mbar_arrive_expect_tx(&sh.full[slot], kDqABytes);
                     for (int hb = 0; hb < 2; ++hb)
                         tma_load_2d(sb + hb * 8192, &map_ds, hb * 64, t * p.Rp + kc * 64, &sh.full[slot]);
-                    const int* ix = sh.idx;
-                    for (int db = 0; db < 4; ++db)
-                        for (int q4 = 0; q4 < 16; ++q4)
-                            tma_gather4(sb + kDqABytes + db * 8192 + q4 * 512, &map_kv,
-                                        half * 256 + db * 64, ix[4 * q4], ix[4 * q4 + 1],
-                                        ix[4 * q4 + 2], ix[4 * q4 + 3], &sh.full[slot]);
                     ++issued;
+                    advance(slot, phase, kDqSlots);
                 }
-                if (++slot == kDqSlots) { slot = 0; phase ^= 1u; }
-                __syncwarp();
+                SMLA_TRACE_EV(1, it, 1);
+            }
+            if (sh.abort_flag) {
+                int s = slot; uint32_t ph = phase;
+                for (int k = 0; k < kDqSlots && k < issued; ++k) {
+                    if (--s < 0) { s = kDqSlots - 1; ph ^= 1u; }
+                    mbar_wait(&sh.full[s], ph, kWaitNs / 8);
+                }
             }
         }
-        if (lane == 0 && sh.abort_flag) {
-            int s = slot; uint32_t ph = phase;
-            for (int k = 0; k < kDqSlots && k < issued; ++k) {
-                if (--s < 0) { s = kDqSlots - 1; ph ^= 1u; }
-                mbar_wait(&sh.full[s], ph, kWaitNs / 8);
+        __syncwarp();
+    } else if (warp >= 6) {
+        // ------------------------------------------------ kv gather (cp.async)
+        // Per 64-rank chunk, copy warp gw copies rows 16gw .. 16gw + 15, one row
+        // per round: lane l copies the 16-byte piece (l & 7) of 64-column block
+        // (l >> 3) of the row's half of D. Lane i < 16 holds the index of row
+        // 16gw + i; indices are loaded two chunks ahead over this CTA's whole
+        // chunk sequence, and pending copies carry over from item to item.
+        const int gw = warp - 6;
+        const int db = lane >> 3, piece = lane & 7;
+        int slot = 0; uint32_t phase = 0;
+        bool ok = true;
+        const int my_items =
+            int(blockIdx.x) < nitems ? (nitems - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
+        const int nchunks = my_items * nkc;
+        auto load_idx = [&](int n) -> int {
+            if (n >= nchunks) return 0;
+            const int item = blockIdx.x + (n / nkc) * int(gridDim.x);
+            const int rl = (n % nkc) * 64 + 16 * gw + (lane & 15);
+            int j = 0;
+            if (rl < p.R) {
+                j = __ldg(p.topk + int64_t(item >> 1) * p.K + p.r0 + rl);
+                if (j < 0 || j >= p.N) j = 0;      // masked or invalid: its dS is zero
             }
+            return j;
+        };
+        int i0 = load_idx(0), i1 = load_idx(1);
+        int pend[kDqSlots] = {0, 0, 0, 0};
+        int npend = 0;
+        auto flush_one = [&]() {
+            fence_proxy_async_smem();
+            mbar_arrive(&sh.full[pend[0]]);
+#pragma unroll
+            for (int k = 0; k + 1 < kDqSlots; ++k) pend[k] = pend[k + 1];
+            --npend;
+        };
+        for (int n = 0; n < nchunks && ok; ++n) {
+            const int item = blockIdx.x + (n / nkc) * int(gridDim.x);
+            const int i2 = load_idx(n + 2);
+            if (lane == 0) ok = wait_or_abort(&sh.empty[slot], phase ^ 1u, &sh.abort_flag, p.status);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            const char* src0 =
+                reinterpret_cast<const char*>(p.kv) + ((item & 1) * 256 + db * 64) * 2 + piece * 16;
+            uint8_t* bt = slots + slot * kDqSlotBytes + kDqABytes + db * 8192;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int r = 16 * gw + i;
+                const int j = __shfl_sync(0xffffffffu, i0, i);
+                cp_async16(bt + r * 128 + ((piece ^ (r & 7)) << 4), src0 + int64_t(j) * (kD * 2));
+            }
+            cp_async_commit();
+            pend[npend++] = slot;
+            if (npend == kDqSlots - 1) { cp_async_wait<kDqSlots - 2>(); flush_one(); }
+            advance(slot, phase, kDqSlots);
+            i0 = i1;
+            i1 = i2;
         }
+        cp_async_wait<0>();
+        while (npend > 0) flush_one();
     } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             int slot = 0; uint32_t phase = 0;
             bool ok = true;
@@ -467,28 +683,30 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const __grid_constant__ CU
             for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
                 const int b = it & 1;
                 if (it >= 2) ok = wait_or_abort(&sh.d_empty[b], ((it >> 1) - 1) & 1, &sh.abort_flag, p.status);
+                SMLA_TRACE_EV(1, it, 2);
                 for (int kc = 0; kc < nkc && ok; ++kc) {
                     ok = wait_or_abort(&sh.full[slot], phase, &sh.abort_flag, p.status);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t sb = smem_u32(slots + slot * kDqSlotBytes);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t ad = sdesc_sw128(sb + ks * 2048, 8192, 1024);
-                        const uint64_t bd = sdesc_sw128(sb + kDqABytes + ks * 2048, 8192, 1024);
-                        mma_ss(tbase + 256 * b, ad, bd, kDqIdesc, (kc | ks) != 0);
-                    }
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ss(tbase + 256 * b, sdesc_sw128(sb + ks * 2048, 8192, 1024),
+                               sdesc_sw128(sb + kDqABytes + ks * 2048, 8192, 1024), kDqIdesc,
+                               (kc | ks) != 0);
                     mma_commit(&sh.empty[slot]);
-                    if (++slot == kDqSlots) { slot = 0; phase ^= 1u; }
+                    advance(slot, phase, kDqSlots);
                 }
                 if (!ok) break;
                 mma_commit(&sh.d_full[b]);
+                SMLA_TRACE_EV(1, it, 3);
             }
             mma_commit(&sh.drain);
             mbar_wait(&sh.drain, 0, kWaitNs);
         }
         __syncwarp();
     } else {
+        // ----------------------------------------------------------- epilogue
         const int quarter = warp & 3;
         const int h = quarter * 32 + lane;
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
@@ -497,6 +715,7 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const __grid_constant__ CU
             const int t = item >> 1, half = item & 1;
             const int b = it & 1;
             if (!wait_or_abort(&sh.d_full[b], (it >> 1) & 1, &sh.abort_flag, p.status)) break;
+            if (warp == 2 && lane == 0) SMLA_TRACE_EV(1, it, 4);
             tc_fence_after();
             const int64_t base = (int64_t(t) * H + h) * kD + half * 256;
 #pragma unroll 1
@@ -536,6 +755,7 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const __grid_constant__ CU
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.d_empty[b]);
+            if (warp == 2 && lane == 0) SMLA_TRACE_EV(1, it, 5);
         }
     }
     tc_fence_before();
@@ -546,6 +766,7 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const __grid_constant__ CU
     }
 }
 
+// ================================================================= launchers
 int sm_count() {
     static int cached[64];
     int dev = 0;
@@ -575,22 +796,23 @@ cudaError_t launch_sdi_h(const ChunkArgs& a, cudaStream_t s) {
     static bool attr_done[64] = {false};
     if (set_smem_attrs_once(reinterpret_cast<const void*>(sdi_kernel<H>), C::kSmem, attr_done))
         return cudaErrorInvalidValue;
-    CUtensorMap mq, mdo, mkv;
+    const int Rp = round_up_ranks(a.R), Hp = pad_heads(H);
+    CUtensorMap mq, mdo, mim, mds;
     if (!make_tmap_bf16_2d(&mq, a.q, uint64_t(a.T) * H, kD, kD, H, 64, true) ||
         !make_tmap_bf16_2d(&mdo, a.dO, uint64_t(a.T) * H, kD, kD, H, 64, true) ||
-        !make_tmap_bf16_2d(&mkv, a.kv, a.N, kD, kD, 1, 64, true))
+        !make_tmap_bf16_2d(&mim, a.interm, uint64_t(a.T) * a.R, kD, kD, 32, 64, true) ||
+        !make_tmap_bf16_2d(&mds, a.dsT, uint64_t(a.T) * Rp, Hp, Hp, 32, 64, true))
         return cudaErrorInvalidValue;
     SdiParams sp{};
-    sp.topk = a.topk; sp.lse = a.lse; sp.delta = a.delta; sp.interm = a.interm; sp.dsT = a.dsT;
-    sp.T = a.T; sp.K = a.K; sp.N = a.N; sp.r0 = a.r0; sp.R = a.R;
-    sp.Rp = round_up_ranks(a.R); sp.Hp = pad_heads(H);
+    sp.kv = a.kv; sp.topk = a.topk; sp.lse = a.lse; sp.delta = a.delta; sp.interm = a.interm;
+    sp.T = a.T; sp.K = a.K; sp.N = a.N; sp.r0 = a.r0; sp.R = a.R; sp.Rp = Rp; sp.Hp = Hp;
     sp.npairs = (a.R + 255) / 256;
     sp.tiles_last = (a.R - (sp.npairs - 1) * 256) > 128 ? 2 : 1;
     sp.scale = a.scale; sp.status = a.status;
     const int64_t items = int64_t(a.T) * sp.npairs;
     const int sms = sm_count();
     const int grid = int(items < sms ? items : sms);
-    sdi_kernel<H><<<grid, C::kThreads, C::kSmem, s>>>(mq, mdo, mkv, sp);
+    sdi_kernel<H><<<grid, C::kThreads, C::kSmem, s>>>(mq, mdo, mim, mds, sp);
     note_launch();
     return cudaGetLastError();
 }
@@ -600,37 +822,44 @@ cudaError_t launch_dq_h(const ChunkArgs& a, cudaStream_t s) {
     static bool attr_done[64] = {false};
     if (set_smem_attrs_once(reinterpret_cast<const void*>(dq_kernel<H>), kDqSmem, attr_done))
         return cudaErrorInvalidValue;
-    const int Rp = round_up_ranks(a.R);
-    const int Hp = pad_heads(H);
-    CUtensorMap mds, mkv;
-    if (!make_tmap_bf16_2d(&mds, a.dsT, uint64_t(a.T) * Rp, Hp, Hp, 64, 64, true) ||
-        !make_tmap_bf16_2d(&mkv, a.kv, a.N, kD, kD, 1, 64, true))
+    const int Rp = round_up_ranks(a.R), Hp = pad_heads(H);
+    CUtensorMap mds;
+    if (!make_tmap_bf16_2d(&mds, a.dsT, uint64_t(a.T) * Rp, Hp, Hp, 64, 64, true))
         return cudaErrorInvalidValue;
     DqParams dp{};
-    dp.topk = a.topk; dp.dq_acc = a.dq_acc; dp.dq_out = a.dq_out;
+    dp.kv = a.kv; dp.topk = a.topk; dp.dq_acc = a.dq_acc; dp.dq_out = a.dq_out;
     dp.T = a.T; dp.K = a.K; dp.N = a.N; dp.r0 = a.r0; dp.R = a.R; dp.Rp = Rp;
     dp.first = a.first_chunk; dp.last = a.last_chunk; dp.status = a.status;
     const int64_t items = int64_t(a.T) * 2;
     const int sms = sm_count();
     const int grid = int(items < sms ? items : sms);
-    dq_kernel<H><<<grid, 192, kDqSmem, s>>>(mds, mkv, dp);
+    dq_kernel<H><<<grid, 320, kDqSmem, s>>>(mds, dp);
     note_launch();
     return cudaGetLastError();
 }
 
 }  // namespace
 
-#define SMLA_DISPATCH_H(FN, a, s)                     \
-    switch ((a).H) {                                  \
-        case 16: return FN<16>(a, s);                 \
-        case 32: return FN<32>(a, s);                 \
-        case 48: return FN<48>(a, s);                 \
-        case 64: return FN<64>(a, s);                 \
-        case 80: return FN<80>(a, s);                 \
-        case 96: return FN<96>(a, s);                 \
-        case 112: return FN<112>(a, s);               \
-        case 128: return FN<128>(a, s);               \
-        default: return cudaErrorInvalidValue;        \
+#ifdef SMLA_TRACE
+extern "C" int smla_trace_copy(unsigned long long* host, size_t count) {
+    const size_t n = sizeof(g_smla_trace) / sizeof(g_smla_trace[0]);
+    return cudaMemcpyFromSymbol(host, g_smla_trace,
+                                sizeof(unsigned long long) * (count < n ? count : n)) == cudaSuccess
+               ? 0 : 1;
+}
+#endif
+
+#define SMLA_DISPATCH_H(FN, a, s)              \
+    switch ((a).H) {                           \
+        case 16: return FN<16>(a, s);          \
+        case 32: return FN<32>(a, s);          \
+        case 48: return FN<48>(a, s);          \
+        case 64: return FN<64>(a, s);          \
+        case 80: return FN<80>(a, s);          \
+        case 96: return FN<96>(a, s);          \
+        case 112: return FN<112>(a, s);        \
+        case 128: return FN<128>(a, s);        \
+        default: return cudaErrorInvalidValue; \
     }
 
 cudaError_t launch_attn_sdi(const ChunkArgs& a, cudaStream_t s) {
