@@ -1,0 +1,84 @@
+"""GPU parity at the full workload sizes, in the launch configuration bench.py
+times (same shapes, same rank chunking), on outputs the fp64 oracle can
+compute one by one:
+
+* dq for a sample of tokens (the first and last tokens, the end of the short
+  windows, and seeded random tokens);
+* dkv for a sample of kv rows (window rows, pool rows, and the rows with the
+  most contributors -- the hottest Zipf rows in the skewed workload), each
+  computed by the oracle from its full contributor list;
+* all of d_sink;
+plus bitwise run-to-run determinism of dq, dkv and d_sink.
+
+O and lse, the backward's inputs, come from the oracle's forward over all
+tokens (never from the CUDA path).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_mla_attention_gb300 as smla
+from sparse_mla_attention_gb300 import workloads as W
+from gpu_helpers import Case, compare, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from sparse_mla_attention_gb300 import build
+    build.build()
+    oracle.build()
+    assert torch.cuda.is_available()
+
+
+def _sample_tokens(T, rng, n=40):
+    fixed = [0, 1, 2, 63, 126, 127, 128, T // 2, T - 2, T - 1]
+    rest = rng.choice(T, size=n - len(fixed), replace=False)
+    return np.unique(np.concatenate([fixed, rest]).astype(np.int64))
+
+
+def _sample_rows(topk, N, T, rng, n=32):
+    counts = np.bincount(topk[topk >= 0], minlength=N)
+    hottest = np.argsort(-counts, kind="stable")[:6]
+    window = rng.choice(T, size=8, replace=False)
+    pool = T + rng.choice(N - T, size=8, replace=False) if N > T else np.array([], np.int64)
+    unused = np.flatnonzero(counts == 0)[:2]
+    fixed = [0, T - 1, N - 1]
+    rows = np.concatenate([hottest, window, pool, unused, fixed]).astype(np.int64)
+    return np.unique(rows)
+
+
+@pytest.mark.parametrize("name", ["headline", "headline_h64_chunked", "t8192_zipf"])
+def test_full_size_sampled_parity_and_determinism(name):
+    spec = W.WORKLOADS[name]
+    inp = W.make_inputs(spec)
+    c = Case(inp)
+    r_chunk = spec.r_chunk or None
+    ws = smla.Workspace()
+    out1 = smla.sparse_mla_bwd(c.q, c.kv, c.do, c.o, c.lse, c.topk, c.sink, scale=c.scale,
+                               r_chunk=r_chunk, workspace=ws)
+    out2 = smla.sparse_mla_bwd(c.q, c.kv, c.do, c.o, c.lse, c.topk, c.sink, scale=c.scale,
+                               r_chunk=r_chunk, workspace=ws)
+    torch.cuda.synchronize()
+    for a, b in zip(out1, out2):
+        if a is not None:
+            assert torch.equal(a, b), "run-to-run results differ"
+    dq, dkv, dsink = out1
+
+    rng = np.random.default_rng(123)
+    toks = _sample_tokens(spec.T, rng)
+    ref_dq = c.ref_dq(toks)
+    compare(f"{name} dq[sampled tokens]", to_f64(dq[torch.from_numpy(toks).cuda()]), ref_dq)
+
+    rows = _sample_rows(inp["topk"], spec.num_kv, spec.T, rng)
+    ref_dkv = oracle.dkv_rows(c.q64, c.kv64, c.do64, c.o64, c.lse64, inp["topk"], c.scale, rows,
+                              r_chunk=spec.r_chunk or None)
+    compare(f"{name} dkv[sampled rows]", to_f64(dkv[torch.from_numpy(rows).cuda()]), ref_dkv)
+
+    if c.sink is not None:
+        compare(f"{name} d_sink", to_f64(dsink), c.ref_dsink())
+    else:
+        assert dsink is None
