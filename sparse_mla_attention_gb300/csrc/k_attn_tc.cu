@@ -378,6 +378,8 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         const int r = quarter * 32 + lane;              // TMEM lane = rank inside the tile
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
         uint8_t* stage = slots + C::kSlots * C::kSlotBytes + (warp - 2) * kStageBytes;
+        float* lsd = reinterpret_cast<float*>(stage);   // [0, H): lse*log2(e); [H, 2H): delta
+        static_assert(2 * H * 4 <= kStageBytes, "lse / delta must fit the staging tile");
         const float c1 = p.scale * kLog2e;
         constexpr int kHw = (H + 31) / 32;              // head words per lane
         uint32_t x_use = 0;                             // accumulations of this tile consumed
@@ -402,8 +404,20 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 const int j = __ldg(p.topk + int64_t(t) * p.K + p.r0 + rl);
                 valid = j >= 0 && j < p.N;
             }
+            // lse * log2(e) and delta of every head go to the head of this warp's
+            // staging tile (free once its last TMA store has read it), from where
+            // each lane reads them as shared-memory broadcasts
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < kHw; ++k) {
+                const int h = k * 32 + lane;
+                if (h < H) { lsd[h] = lse_w[k]; lsd[H + h] = del_w[k]; }
+            }
+            __syncwarp();
             if (!wait_or_abort(&sh.s_full, it & 1, &sh.abort_flag, p.status)) break;
             if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 7);
+            __syncwarp();
             tc_fence_after();
             if (active) {
                 const uint32_t trow = tbase + lane_off + g * 256;
@@ -422,15 +436,22 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         if (u >= nch) break;
+                        float l2v[16], dev[16];
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const float4 a = reinterpret_cast<const float4*>(lsd + (c16 + u) * 16)[v];
+                            const float4 b = reinterpret_cast<const float4*>(lsd + H + (c16 + u) * 16)[v];
+                            l2v[4 * v] = a.x; l2v[4 * v + 1] = a.y; l2v[4 * v + 2] = a.z; l2v[4 * v + 3] = a.w;
+                            dev[4 * v] = b.x; dev[4 * v + 1] = b.y; dev[4 * v + 2] = b.z; dev[4 * v + 3] = b.w;
+                        }
                         uint32_t pp[8];
 #pragma unroll
                         for (int j2 = 0; j2 < 8; ++j2) {
                             float pv[2], dsv[2];
 #pragma unroll
                             for (int e = 0; e < 2; ++e) {
-                                const int h = (c16 + u) * 16 + 2 * j2 + e;
-                                const float l2 = __shfl_sync(0xffffffffu, lse_w[h >> 5], h & 31);
-                                const float de = __shfl_sync(0xffffffffu, del_w[h >> 5], h & 31);
+                                const float l2 = l2v[2 * j2 + e];
+                                const float de = dev[2 * j2 + e];
                                 const float s = __uint_as_float(sv[u][2 * j2 + e]);
                                 const float dp = __uint_as_float(dv[u][2 * j2 + e]);
                                 const float pe = valid ? exp2f(fmaf(s, c1, -l2)) : 0.f;
@@ -479,8 +500,10 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 if (!wait_or_abort(&sh.x_full[g], x_use & 1u, &sh.abort_flag, p.status)) { ok = false; break; }
                 ++x_use;
                 if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 32 + c);
+                __syncwarp();
                 tc_fence_after();
                 for (int hh = 0; hh < 2; ++hh) {
+                    __syncwarp();           // lane 0 may still be in the previous half's store
                     const uint32_t xa = tbase + lane_off + g * 256 + 128 + 64 * hh;
                     uint32_t v0[32], v1[32];
                     tmem_ld32(xa, v0);
@@ -716,6 +739,7 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
             const int b = it & 1;
             if (!wait_or_abort(&sh.d_full[b], (it >> 1) & 1, &sh.abort_flag, p.status)) break;
             if (warp == 2 && lane == 0) SMLA_TRACE_EV(1, it, 4);
+            __syncwarp();                   // tcgen05.ld is warp-collective
             tc_fence_after();
             const int64_t base = (int64_t(t) * H + h) * kD + half * 256;
 #pragma unroll 1
@@ -751,6 +775,7 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
                                               pack_bf16x2(f[8 * k + 6], f[8 * k + 7]));
                     }
                 }
+                __syncwarp();               // lanes with h >= H rejoin before the next load
             }
             tc_fence_before();
             __syncwarp();
