@@ -23,8 +23,9 @@
 //    128-column accumulator; the tiles alternate so that one tile's drain
 //    (TMEM -> bf16 -> staging -> TMA store) overlaps the other tile's MMAs.
 // TMEM (512 columns): tile g owns columns [256g, 256g + 256): S^T | dP^T in
-// [0, 2H); then P^T in [0, H/2), scale*dS^T in [H/2, H) and the interm
-// accumulator in [128, 256).
+// [0, 2H); then, per 16-head chunk k, P^T in [16k, 16k + 8) and scale*dS^T in
+// [16k + 8, 16k + 16) (bf16 pairs over the chunk's own S^T columns), and the
+// interm accumulator in [128, 256).
 //
 // dq_kernel: persistent; item = (token, half of D). dq = (scale*dS) x kv:
 // M = 128 (heads, zero-padded), N = 256, K = ranks in 64-rank steps, both
@@ -349,7 +350,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                         for (int ks = 0; ks < 2 * H / 16; ++ks) {
                             const bool pterm = ks < H / 16;
                             const int kk = pterm ? ks : ks - H / 16;
-                            const uint32_t acol = pterm ? kk * 8 : H / 2 + kk * 8;
+                            const uint32_t acol = kk * 16 + (pterm ? 0 : 8);
                             // dO (P term) or q (dS term): two 64-column blocks of H rows
                             const uint32_t bt = (pterm ? sb + 2 * C::kQBytes : sb) + kk * 2048;
                             mma_ts(tile + 128, tile + acol, sdesc_sw128(bt, C::kQBytes, 1024),
@@ -417,11 +418,11 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             __syncwarp();
             if (!wait_or_abort(&sh.s_full, it & 1, &sh.abort_flag, p.status)) break;
             if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 7);
+            if (warp == 9 && lane == 0) SMLA_TRACE_EV(0, it, 44);
             __syncwarp();
             tc_fence_after();
             if (active) {
                 const uint32_t trow = tbase + lane_off + g * 256;
-                uint32_t dsp[H / 2];
 #pragma unroll
                 for (int c16 = 0; c16 < H / 16; c16 += 2) {
                     const int nch = (c16 + 1 < H / 16) ? 2 : 1;
@@ -433,53 +434,65 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                             tmem_ld16(trow + H + (c16 + u) * 16, dv[u]);
                         }
                     tmem_wait_ld();
+                    if (c16 == 0 && warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 10);
+                    if (c16 == 0 && warp == 9 && lane == 0) SMLA_TRACE_EV(0, it, 60);
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         if (u >= nch) break;
+                        const int k = c16 + u;              // head chunk: heads 16k .. 16k + 15
                         float l2v[16], dev[16];
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
-                            const float4 a = reinterpret_cast<const float4*>(lsd + (c16 + u) * 16)[v];
-                            const float4 b = reinterpret_cast<const float4*>(lsd + H + (c16 + u) * 16)[v];
+                            const float4 a = reinterpret_cast<const float4*>(lsd + k * 16)[v];
+                            const float4 b = reinterpret_cast<const float4*>(lsd + H + k * 16)[v];
                             l2v[4 * v] = a.x; l2v[4 * v + 1] = a.y; l2v[4 * v + 2] = a.z; l2v[4 * v + 3] = a.w;
                             dev[4 * v] = b.x; dev[4 * v + 1] = b.y; dev[4 * v + 2] = b.z; dev[4 * v + 3] = b.w;
                         }
-                        uint32_t pp[8];
+                        uint32_t pp[8], dd[8];
 #pragma unroll
                         for (int j2 = 0; j2 < 8; ++j2) {
                             float pv[2], dsv[2];
 #pragma unroll
                             for (int e = 0; e < 2; ++e) {
-                                const float l2 = l2v[2 * j2 + e];
-                                const float de = dev[2 * j2 + e];
                                 const float s = __uint_as_float(sv[u][2 * j2 + e]);
                                 const float dp = __uint_as_float(dv[u][2 * j2 + e]);
-                                const float pe = valid ? exp2f(fmaf(s, c1, -l2)) : 0.f;
+                                const float pe = valid ? exp2f(fmaf(s, c1, -l2v[2 * j2 + e])) : 0.f;
                                 pv[e] = pe;
-                                dsv[e] = valid ? p.scale * pe * (dp - de) : 0.f;
+                                dsv[e] = valid ? p.scale * pe * (dp - dev[2 * j2 + e]) : 0.f;
                             }
                             pp[j2] = pack_bf16x2(pv[0], pv[1]);
-                            dsp[(c16 + u) * 8 + j2] = pack_bf16x2(dsv[0], dsv[1]);
+                            dd[j2] = pack_bf16x2(dsv[0], dsv[1]);
                         }
-                        // P^T over S^T columns already read
-                        tmem_st8(trow + (c16 + u) * 8, pp);
+                        // P^T and scale*dS^T of chunk k over its S^T columns, already read
+                        tmem_st8(trow + k * 16, pp);
+                        tmem_st8(trow + k * 16 + 8, dd);
                     }
                 }
-#pragma unroll
-                for (int c16 = 0; c16 < H / 16; ++c16) tmem_st8(trow + H / 2 + c16 * 8, dsp + c16 * 8);
+                if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 11);
+                if (warp == 9 && lane == 0) SMLA_TRACE_EV(0, it, 61);
                 tmem_wait_st();
+                if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 12);
+                if (warp == 9 && lane == 0) SMLA_TRACE_EV(0, it, 62);
                 // stash scale * dS^T for the dq kernel: per 64-head block the warp's 32
-                // rows go through the staging tile and one TMA store (heads >= H are 0)
+                // rows are read back from TMEM, go through the staging tile and leave
+                // in one TMA store (heads >= H are 0)
 #pragma unroll
                 for (int hb = 0; hb < (H + 63) / 64; ++hb) {
+                    uint32_t dsw[32];
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int k = hb * 4 + q4;
+                        if (k < H / 16) tmem_ld8(trow + k * 16 + 8, dsw + 8 * q4);
+                    }
+                    tmem_wait_ld();
                     if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
                     uint4* srow = reinterpret_cast<uint4*>(stage + lane * 128);
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
-                        const int w0 = hb * 32 + 4 * v;
-                        srow[v ^ (lane & 7)] = w0 < H / 2
-                            ? make_uint4(dsp[w0], dsp[w0 + 1], dsp[w0 + 2], dsp[w0 + 3])
+                        const int k = hb * 4 + (v >> 1);
+                        srow[v ^ (lane & 7)] = k < H / 16
+                            ? make_uint4(dsw[4 * v], dsw[4 * v + 1], dsw[4 * v + 2], dsw[4 * v + 3])
                             : make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_smem();
@@ -488,8 +501,11 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                         tma_store_2d(&map_ds, hb * 64, t * p.Rp + row0, stage);
                         bulk_commit();
                     }
+                    __syncwarp();
                 }
             }
+            if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 13);
+            if (warp == 9 && lane == 0) SMLA_TRACE_EV(0, it, 63);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.p_ready);
