@@ -456,7 +456,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                             for (int e = 0; e < 2; ++e) {
                                 const float s = __uint_as_float(sv[u][2 * j2 + e]);
                                 const float dp = __uint_as_float(dv[u][2 * j2 + e]);
-                                const float pe = valid ? exp2f(fmaf(s, c1, -l2v[2 * j2 + e])) : 0.f;
+                                const float pe = valid ? ex2_approx(fmaf(s, c1, -l2v[2 * j2 + e])) : 0.f;
                                 pv[e] = pe;
                                 dsv[e] = valid ? p.scale * pe * (dp - dev[2 * j2 + e]) : 0.f;
                             }
