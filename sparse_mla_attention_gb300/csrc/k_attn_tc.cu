@@ -54,6 +54,20 @@ constexpr int kTraceCtas = 8, kTraceItems = 8, kTraceEvents = 64;
 }  // namespace
 #ifdef SMLA_TRACE
 __device__ unsigned long long g_smla_trace[2 * kTraceCtas * kTraceItems * kTraceEvents];
+// per kernel and CTA (< 1024): start and end time of the CTA's MMA thread
+__device__ unsigned long long g_smla_cta_span[2 * 1024 * 3];
+__device__ __forceinline__ unsigned smla_smid() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
+}
+#define SMLA_TRACE_SPAN(kid, which)                                                         \
+    do {                                                                                    \
+        if (blockIdx.x < 1024) {                                                            \
+            g_smla_cta_span[((kid) * 1024 + blockIdx.x) * 3 + (which)] = globaltimer_ns();  \
+            g_smla_cta_span[((kid) * 1024 + blockIdx.x) * 3 + 2] = smla_smid();             \
+        }                                                                                   \
+    } while (0)
 #define SMLA_TRACE_EV(kid, it, ev)                                                          \
     do {                                                                                    \
         if (blockIdx.x < kTraceCtas && (it) < kTraceItems)                                  \
@@ -63,6 +77,9 @@ __device__ unsigned long long g_smla_trace[2 * kTraceCtas * kTraceItems * kTrace
 #else
 #define SMLA_TRACE_EV(kid, it, ev) \
     do {                           \
+    } while (0)
+#define SMLA_TRACE_SPAN(kid, which) \
+    do {                            \
     } while (0)
 #endif
 namespace {
@@ -287,6 +304,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
+            SMLA_TRACE_SPAN(0, 0);
             int slot = 0; uint32_t phase = 0;
             uint32_t xe_done[2] = {0, 0};   // drains of tile g's accumulator seen
             uint32_t x_uses[2] = {0, 0};    // accumulations of tile g issued
@@ -370,6 +388,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             // every MMA issued by this thread completes before TMEM is freed
             mma_commit(&sh.drain);
             mbar_wait(&sh.drain, 0, kWaitNs);
+            SMLA_TRACE_SPAN(0, 1);
         }
         __syncwarp();
     } else {
@@ -716,6 +735,7 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
+            SMLA_TRACE_SPAN(1, 0);
             int slot = 0; uint32_t phase = 0;
             bool ok = true;
             int it = 0;
@@ -742,6 +762,7 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
             }
             mma_commit(&sh.drain);
             mbar_wait(&sh.drain, 0, kWaitNs);
+            SMLA_TRACE_SPAN(1, 1);
         }
         __syncwarp();
     } else {
@@ -882,6 +903,9 @@ cudaError_t launch_dq_h(const ChunkArgs& a, cudaStream_t s) {
 }  // namespace
 
 #ifdef SMLA_TRACE
+extern "C" int smla_trace_span_copy(unsigned long long* host) {
+    return cudaMemcpyFromSymbol(host, g_smla_cta_span, sizeof(g_smla_cta_span)) == cudaSuccess ? 0 : 1;
+}
 extern "C" int smla_trace_copy(unsigned long long* host, size_t count) {
     const size_t n = sizeof(g_smla_trace) / sizeof(g_smla_trace[0]);
     return cudaMemcpyFromSymbol(host, g_smla_trace,

@@ -148,6 +148,33 @@ int check_arch() {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA; }
 
+// A side stream (and two events) per host thread and device, created on first
+// use: the CSR build of a rank chunk (a chain of small kernels that needs only
+// topk) runs on it, forked from the caller's stream at the start of the chunk
+// and joined back before the chunk's gather, so that it overlaps the delta and
+// attention phases. The caller sees all work ordered on its own stream.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+SideStream* side_stream() {
+    thread_local SideStream per_dev[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) { cudaGetLastError(); return nullptr; }
+    SideStream& ss = per_dev[dev];
+    if (!ss.stream) {
+        if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            ss = SideStream{};
+            return nullptr;
+        }
+    }
+    return &ss;
+}
+
 }  // namespace
 }  // namespace smla
 
@@ -267,19 +294,26 @@ int smla_bwd(const uint16_t* q, const uint16_t* kv, const uint16_t* dO, const ui
     float* dq_acc = plan.nchunks > 1 ? reinterpret_cast<float*>(ws + plan.off_dqacc) : nullptr;
     float* dkv_acc = plan.nchunks > 1 ? reinterpret_cast<float*>(ws + plan.off_dkvacc) : nullptr;
 
-    {
-        prof::Scope ph(prof::kDelta, s);
-        if ((rc = cuda_rc(launch_delta(o, dO, delta, int64_t(d.T) * d.H, s)))) return rc;
-    }
+    SideStream* side = side_stream();
+    if (!side) return SMLA_ERR_CUDA;
     const float scale = eff_scale(d);
     for (int c = 0; c < plan.nchunks; ++c) {
         const int r0 = int(c * plan.R);
         const bool first = c == 0, last = c == plan.nchunks - 1;
+        // CSR of this chunk on the side stream (after the previous chunk's gather,
+        // which read the CSR buffers); joined back before this chunk's gather
+        if ((rc = cuda_rc(cudaEventRecord(side->fork, s)))) return rc;
+        if ((rc = cuda_rc(cudaStreamWaitEvent(side->stream, side->fork, 0)))) return rc;
         {
-            prof::Scope ph(prof::kCsr, s);
+            prof::Scope ph(prof::kCsr, side->stream);
             rc = cuda_rc(launch_csr(topk, d.T, d.topk, r0, int(plan.R), d.num_kv, row_ptr, col,
-                                    ws + plan.off_csr, plan.csr, status, s));
+                                    ws + plan.off_csr, plan.csr, status, side->stream));
             if (rc) return rc;
+        }
+        if ((rc = cuda_rc(cudaEventRecord(side->join, side->stream)))) return rc;
+        if (first) {
+            prof::Scope ph(prof::kDelta, s);
+            if ((rc = cuda_rc(launch_delta(o, dO, delta, int64_t(d.T) * d.H, s)))) return rc;
         }
         ChunkArgs a{};
         a.q = q; a.kv = kv; a.dO = dO; a.lse = lse; a.delta = delta; a.topk = topk;
@@ -294,6 +328,7 @@ int smla_bwd(const uint16_t* q, const uint16_t* kv, const uint16_t* dO, const ui
             prof::Scope ph(prof::kDq, s);
             if ((rc = cuda_rc(launch_attn_dq(a, s)))) return rc;
         }
+        if ((rc = cuda_rc(cudaStreamWaitEvent(s, side->join, 0)))) return rc;
         prof::Scope ph(prof::kGather, s);
         rc = cuda_rc(launch_gather(row_ptr, col, interm, d.num_kv, plan.max_segs,
                                    reinterpret_cast<int32_t*>(ws + plan.off_segcnt),
