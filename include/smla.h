@@ -76,10 +76,12 @@ typedef struct smla_dims {
 } smla_dims;
 
 /* Operation selector for smla_workspace_size. */
-enum smla_op { SMLA_OP_FWD = 0, SMLA_OP_BWD = 1, SMLA_OP_CSR = 2 };
+enum smla_op { SMLA_OP_FWD = 0, SMLA_OP_BWD = 1, SMLA_OP_CSR = 2, SMLA_OP_BWD_HOST = 3 };
 
 /*
- * Workspace bytes needed by one call of `op` with these dimensions.
+ * Workspace bytes needed by one call of `op` with these dimensions
+ * (SMLA_OP_BWD_HOST: smla_bwd_host, the backward's workspace plus device
+ * copies of its inputs and outputs).
  * For SMLA_OP_CSR the fields used are T, topk (the row width of the index
  * table), r_chunk (the number of ranks covered, 0 = topk) and num_kv.
  * Returns SMLA_OK and writes *bytes, or a validation error.
@@ -126,6 +128,32 @@ int smla_bwd(const uint16_t* q, const uint16_t* kv, const uint16_t* dO,
              const float* sink, uint16_t* dq, uint16_t* dkv, float* d_sink,
              const smla_dims* dims, void* workspace, size_t workspace_bytes,
              void* stream);
+
+/*
+ * The same backward with every input and output in HOST memory (the pages
+ * have no such call; it is the end-to-end form of smla_bwd). Arguments,
+ * results and errors are those of smla_bwd, except that q, kv, dO, o, lse,
+ * topk, sink, dq, dkv and d_sink are host pointers (no alignment rule), and the
+ * workspace (device memory, 16-byte aligned) must hold
+ * smla_workspace_size(SMLA_OP_BWD_HOST) bytes: the backward's own workspace
+ * followed by device copies of the inputs and outputs.
+ * The call enqueues work and returns: host-to-device copies run on an internal
+ * copy stream, small inputs first (the CSR build needs only topk), then o, dO
+ * and q in chunks of about 512 tokens; each token chunk's delta, S/dP/dS and dq
+ * start as soon as its inputs have arrived, while later chunks are still
+ * being copied; each chunk's dq goes back to the host on a second copy stream
+ * as soon as it is final, then dkv and d_sink. `stream` waits for all of it:
+ * the host outputs are valid once `stream` (or an event recorded on it after
+ * the call) has completed. Host buffers must stay valid and unchanged until
+ * then. Use page-locked host memory (cudaHostAlloc / cudaHostRegister) for the
+ * copies to run asynchronously; pageable memory also works, with copies that
+ * do not overlap.
+ */
+int smla_bwd_host(const uint16_t* q, const uint16_t* kv, const uint16_t* dO,
+                  const uint16_t* o, const float* lse, const int32_t* topk,
+                  const float* sink, uint16_t* dq, uint16_t* dkv, float* d_sink,
+                  const smla_dims* dims, void* workspace, size_t workspace_bytes,
+                  void* stream);
 
 /*
  * Inverted top-k CSR over the ranks [r0, r0 + r_len) of each row of topk
@@ -177,8 +205,10 @@ int smla_get_device_status(const void* workspace, void* stream, int* status);
 
 /*
  * Phase profiling (tracing aid; off by default). While enabled, smla_bwd
- * brackets each of its phases with CUDA events on the caller's stream and
- * counts the kernels it launches. The aiter page reports a per-kernel sum
+ * brackets each of its phases with CUDA events on the stream that runs it (the
+ * caller's; the CSR build runs on the library's side stream, overlapped with
+ * the others, so its span is not its own run time) and counts the kernels it
+ * launches. The aiter page reports a per-kernel sum
  * next to the end-to-end time (Performance table); these counters give the
  * same split.
  *   smla_profiling(1) enables and resets; smla_profiling(0) disables.

@@ -7,8 +7,8 @@ inputs (``workloads``).
 """
 
 from .api import (Workspace, csr_build, default_scale, device_status, make_dims,
-                  sparse_mla_bwd, sparse_mla_fwd, workspace_size)
+                  sparse_mla_bwd, sparse_mla_bwd_host, sparse_mla_fwd, workspace_size)
 from ._lib import SmlaError
 
 __all__ = ["Workspace", "csr_build", "default_scale", "device_status", "make_dims",
-           "sparse_mla_bwd", "sparse_mla_fwd", "workspace_size", "SmlaError"]
+           "sparse_mla_bwd", "sparse_mla_bwd_host", "sparse_mla_fwd", "workspace_size", "SmlaError"]

@@ -32,9 +32,9 @@ SMLA_ERR_TIMEOUT = 12
 SMLA_ERR_SINK = 13
 SMLA_ERR_ARG = 14
 
-SMLA_OP_FWD, SMLA_OP_BWD, SMLA_OP_CSR = 0, 1, 2
+SMLA_OP_FWD, SMLA_OP_BWD, SMLA_OP_CSR, SMLA_OP_BWD_HOST = 0, 1, 2, 3
 
-EXPORTED = ("smla_workspace_size", "smla_fwd", "smla_bwd", "smla_csr_build",
+EXPORTED = ("smla_workspace_size", "smla_fwd", "smla_bwd", "smla_bwd_host", "smla_csr_build",
             "smla_get_device_status", "smla_status_string", "smla_version",
             "smla_profiling", "smla_profile_read", "smla_dsink_static")
 
@@ -79,6 +79,7 @@ def load(path: str = LIB_PATH):
         lib.smla_workspace_size.argtypes = [ctypes.c_int, dims_p, ctypes.POINTER(sz)]
         lib.smla_fwd.argtypes = [vp] * 6 + [dims_p, vp, sz, vp]
         lib.smla_bwd.argtypes = [vp] * 10 + [dims_p, vp, sz, vp]
+        lib.smla_bwd_host.argtypes = [vp] * 10 + [dims_p, vp, sz, vp]
         lib.smla_csr_build.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, sz, vp]
         lib.smla_get_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
         lib.smla_dsink_static.argtypes = [vp] * 5 + [i32, i32, vp]
@@ -87,7 +88,7 @@ def load(path: str = LIB_PATH):
                                           ctypes.POINTER(ctypes.c_int)]
         lib.smla_status_string.argtypes = [ctypes.c_int]
         lib.smla_status_string.restype = ctypes.c_char_p
-        for name in ("smla_workspace_size", "smla_fwd", "smla_bwd", "smla_csr_build",
+        for name in ("smla_workspace_size", "smla_fwd", "smla_bwd", "smla_bwd_host", "smla_csr_build",
                      "smla_get_device_status", "smla_version", "smla_profiling",
                      "smla_profile_read", "smla_dsink_static"):
             getattr(lib, name).restype = ctypes.c_int

@@ -17,7 +17,7 @@ from typing import Optional, Tuple
 import torch
 
 from . import _lib
-from ._lib import SmlaDims, SMLA_OP_BWD, SMLA_OP_CSR, SMLA_OP_FWD
+from ._lib import SmlaDims, SMLA_OP_BWD, SMLA_OP_BWD_HOST, SMLA_OP_CSR, SMLA_OP_FWD
 
 D_HEAD = 512
 
@@ -149,6 +149,78 @@ def sparse_mla_bwd(q: torch.Tensor, kv: torch.Tensor, do: torch.Tensor, o: torch
         st = device_status(ws)
         if st != _lib.SMLA_OK:
             raise _lib.SmlaError(st, "smla_bwd (device)")
+    return dq, dkv, d_sink
+
+
+def _need_host(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def sparse_mla_bwd_host(q: torch.Tensor, kv: torch.Tensor, do: torch.Tensor, o: torch.Tensor,
+                        lse: torch.Tensor, topk: torch.Tensor, sink: Optional[torch.Tensor] = None,
+                        scale: Optional[float] = None, r_chunk: Optional[int] = None,
+                        workspace: Optional[Workspace] = None, out=None, device=None,
+                        synchronize: bool = True, check_status: bool = True):
+    """Backward with host (CPU) inputs and outputs, through smla_bwd_host.
+
+    The library copies the inputs to the device in token chunks, overlapping
+    the copies with the compute, and copies dq, dkv and d_sink back. Pinned
+    host tensors (``tensor.pin_memory()``) let the copies run asynchronously.
+    ``out`` may pass preallocated host (dq, dkv, d_sink). With ``synchronize``
+    the call waits for the results (and, with ``check_status``, raises if a
+    kernel met an out-of-range index); without it the results are valid once
+    the current CUDA stream of ``device`` has completed.
+    """
+    _need_host(q, "q", torch.bfloat16, 3)
+    _need_host(kv, "kv", torch.bfloat16, 2)
+    _need_host(do, "do", torch.bfloat16, 3)
+    _need_host(o, "o", torch.bfloat16, 3)
+    _need_host(lse, "lse", torch.float32, 2)
+    _need_host(topk, "topk", torch.int32, 2)
+    T, H, D = q.shape
+    if do.shape != q.shape or o.shape != q.shape:
+        raise ValueError("do and o must have the shape of q")
+    if tuple(lse.shape) != (T, H):
+        raise ValueError("lse must have shape [T, H]")
+    if kv.shape[1] != D or topk.shape[0] != T:
+        raise ValueError("shape mismatch between q, kv and topk")
+    if sink is not None:
+        _need_host(sink, "sink", torch.float32, 1)
+        if sink.shape[0] != H:
+            raise ValueError("sink must have shape [H]")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    dims = make_dims(T, H, topk.shape[1], kv.shape[0], r_chunk or 0, scale, D)
+    ws = (workspace or Workspace(dev)).get(workspace_size(SMLA_OP_BWD_HOST, dims))
+    if out is None:
+        pin = q.is_pinned()
+        dq = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin)
+        dkv = torch.empty(kv.shape, dtype=kv.dtype, pin_memory=pin)
+        d_sink = None if sink is None else torch.empty(H, dtype=torch.float32, pin_memory=pin)
+    else:
+        dq, dkv, d_sink = out
+        _need_host(dq, "dq", torch.bfloat16, 3)
+        _need_host(dkv, "dkv", torch.bfloat16, 2)
+        if d_sink is not None:
+            _need_host(d_sink, "d_sink", torch.float32, 1)
+    _lib.check(_lib.load().smla_bwd_host(_ptr(q), _ptr(kv), _ptr(do), _ptr(o), _ptr(lse), _ptr(topk),
+                                         _ptr(sink), _ptr(dq), _ptr(dkv), _ptr(d_sink),
+                                         ctypes.byref(dims), _ptr(ws), ws.numel(), _stream(dev)),
+               "smla_bwd_host")
+    if synchronize:
+        torch.cuda.current_stream(dev).synchronize()
+        if check_status:
+            st = device_status(ws)
+            if st != _lib.SMLA_OK:
+                raise _lib.SmlaError(st, "smla_bwd_host (device)")
     return dq, dkv, d_sink
 
 

@@ -175,6 +175,159 @@ SideStream* side_stream() {
     return &ss;
 }
 
+
+// Device pointers of one backward call.
+struct BwdArgs {
+    const uint16_t* q; const uint16_t* kv; const uint16_t* dO; const uint16_t* o;
+    const float* lse; const int32_t* topk; const float* sink;
+    uint16_t* dq; uint16_t* dkv; float* d_sink;
+};
+
+// Optional token pipelining of a call whose inputs arrive in token chunks:
+// before its first use of tokens [t[i], t[i+1]) the compute stream waits for
+// in_ready[i]; after their final dq it records dq_ready[i].
+struct TokenFeed {
+    int n;
+    const int* t;
+    cudaEvent_t* in_ready;
+    cudaEvent_t* dq_ready;
+};
+
+// Enqueues the whole backward on stream s (validation done by the caller).
+int enqueue_bwd(const BwdArgs& A, const smla_dims& d, const BwdPlan& plan, char* ws,
+                cudaStream_t s, const TokenFeed* feed) {
+    int rc = SMLA_OK;
+    unsigned* status = reinterpret_cast<unsigned*>(ws);
+    if ((rc = cuda_rc(cudaMemsetAsync(status, 0, sizeof(unsigned), s)))) return rc;
+    if (d.T == 0) {
+        if ((rc = cuda_rc(cudaMemsetAsync(A.dkv, 0, size_t(d.num_kv) * kD * 2, s)))) return rc;
+        if (A.d_sink) return cuda_rc(cudaMemsetAsync(A.d_sink, 0, size_t(d.H) * 4, s));
+        return SMLA_OK;
+    }
+    float* delta = reinterpret_cast<float*>(ws + plan.off_delta);
+    int32_t* row_ptr = reinterpret_cast<int32_t*>(ws + plan.off_rowptr);
+    int32_t* col = reinterpret_cast<int32_t*>(ws + plan.off_col);
+    uint16_t* interm = reinterpret_cast<uint16_t*>(ws + plan.off_interm);
+    uint16_t* dsT = reinterpret_cast<uint16_t*>(ws + plan.off_dst);
+    float* dq_acc = plan.nchunks > 1 ? reinterpret_cast<float*>(ws + plan.off_dqacc) : nullptr;
+    float* dkv_acc = plan.nchunks > 1 ? reinterpret_cast<float*>(ws + plan.off_dkvacc) : nullptr;
+    const int64_t Rp = round_up_ranks(int(plan.R)), Hp = pad_heads(d.H);
+    const int whole[2] = {0, d.T};
+    const int nt = feed ? feed->n : 1;
+    const int* tb = feed ? feed->t : whole;
+
+    SideStream* side = side_stream();
+    if (!side) return SMLA_ERR_CUDA;
+    const float scale = eff_scale(d);
+    for (int c = 0; c < plan.nchunks; ++c) {
+        const int r0 = int(c * plan.R);
+        const bool first = c == 0, last = c == plan.nchunks - 1;
+        // CSR of this chunk on the side stream (after the previous chunk's gather,
+        // which read the CSR buffers); joined back before this chunk's gather
+        if ((rc = cuda_rc(cudaEventRecord(side->fork, s)))) return rc;
+        if ((rc = cuda_rc(cudaStreamWaitEvent(side->stream, side->fork, 0)))) return rc;
+        {
+            prof::Scope ph(prof::kCsr, side->stream);
+            rc = cuda_rc(launch_csr(A.topk, d.T, d.topk, r0, int(plan.R), d.num_kv, row_ptr, col,
+                                    ws + plan.off_csr, plan.csr, status, side->stream));
+            if (rc) return rc;
+        }
+        if ((rc = cuda_rc(cudaEventRecord(side->join, side->stream)))) return rc;
+        for (int i = 0; i < nt; ++i) {
+            const int t0 = tb[i], t1 = tb[i + 1];
+            if (t1 <= t0) continue;
+            const int64_t th = int64_t(t0) * d.H;
+            if (first && feed && (rc = cuda_rc(cudaStreamWaitEvent(s, feed->in_ready[i], 0)))) return rc;
+            if (first) {
+                prof::Scope ph(prof::kDelta, s);
+                if ((rc = cuda_rc(launch_delta(A.o + th * kD, A.dO + th * kD, delta + th,
+                                               int64_t(t1 - t0) * d.H, s)))) return rc;
+            }
+            ChunkArgs a{};
+            a.q = A.q + th * kD; a.kv = A.kv; a.dO = A.dO + th * kD; a.lse = A.lse + th;
+            a.delta = delta + th; a.topk = A.topk + int64_t(t0) * d.topk;
+            a.T = t1 - t0; a.H = d.H; a.K = d.topk; a.N = d.num_kv; a.r0 = r0; a.R = int(plan.R);
+            a.scale = scale;
+            a.interm = interm + int64_t(t0) * plan.R * kD;
+            a.dsT = dsT + int64_t(t0) * Rp * Hp;
+            a.dq_acc = dq_acc ? dq_acc + th * kD : nullptr;
+            a.dq_out = A.dq + th * kD;
+            a.first_chunk = first; a.last_chunk = last; a.status = status;
+            {
+                prof::Scope ph(prof::kSdi, s);
+                if ((rc = cuda_rc(launch_attn_sdi(a, s)))) return rc;
+            }
+            {
+                prof::Scope ph(prof::kDq, s);
+                if ((rc = cuda_rc(launch_attn_dq(a, s)))) return rc;
+            }
+            if (last && feed && (rc = cuda_rc(cudaEventRecord(feed->dq_ready[i], s)))) return rc;
+        }
+        if ((rc = cuda_rc(cudaStreamWaitEvent(s, side->join, 0)))) return rc;
+        prof::Scope ph(prof::kGather, s);
+        rc = cuda_rc(launch_gather(row_ptr, col, interm, d.num_kv, plan.max_segs,
+                                   reinterpret_cast<int32_t*>(ws + plan.off_segcnt),
+                                   reinterpret_cast<int32_t*>(ws + plan.off_segptr),
+                                   reinterpret_cast<int32_t*>(ws + plan.off_segrow),
+                                   ws + plan.off_scan_tmp2,
+                                   reinterpret_cast<float*>(ws + plan.off_partial), dkv_acc, A.dkv,
+                                   first, last, s));
+        if (rc) return rc;
+    }
+    if (A.sink) {
+        prof::Scope ph(prof::kDsink, s);
+        if ((rc = cuda_rc(launch_dsink(delta, A.lse, A.sink, A.d_sink, d.T, d.H, s)))) return rc;
+    }
+    return SMLA_OK;
+}
+
+// Copy streams of the host-buffer entry point (per host thread and device):
+// host-to-device and device-to-host copies each get a stream of their own so
+// that they overlap each other and the compute stream.
+constexpr int kMaxTokenChunks = 32;
+struct HostStreams {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t fork = nullptr, small_in = nullptr, done = nullptr, out_done = nullptr;
+    cudaEvent_t in_ready[kMaxTokenChunks] = {}, dq_ready[kMaxTokenChunks] = {};
+};
+
+HostStreams* host_streams() {
+    thread_local HostStreams per_dev[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) { cudaGetLastError(); return nullptr; }
+    HostStreams& h = per_dev[dev];
+    if (!h.in) {
+        bool ok = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) == cudaSuccess;
+        cudaEvent_t* evs[] = {&h.fork, &h.small_in, &h.done, &h.out_done};
+        for (cudaEvent_t* e : evs)
+            ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+        for (int i = 0; i < kMaxTokenChunks; ++i)
+            ok = ok && cudaEventCreateWithFlags(&h.in_ready[i], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&h.dq_ready[i], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) { cudaGetLastError(); h = HostStreams{}; return nullptr; }
+    }
+    return &h;
+}
+
+// Device copies of the inputs and outputs of the host-buffer entry point,
+// placed after the backward's own workspace.
+struct HostPlan {
+    size_t off_q, off_kv, off_dO, off_o, off_lse, off_topk, off_sink, off_dq, off_dkv, off_dsink, bytes;
+};
+
+HostPlan plan_host(const smla_dims& d, const BwdPlan& bp) {
+    HostPlan h{};
+    size_t off = align_up(bp.bytes, 256);
+    auto take = [&](size_t bytes) { size_t o = off; off += align_up(bytes > 0 ? bytes : 1, 256); return o; };
+    const size_t thd = size_t(d.T) * d.H * kD * 2, th4 = size_t(d.T) * d.H * 4;
+    h.off_q = take(thd); h.off_kv = take(size_t(d.num_kv) * kD * 2); h.off_dO = take(thd);
+    h.off_o = take(thd); h.off_lse = take(th4); h.off_topk = take(size_t(d.T) * d.topk * 4);
+    h.off_sink = take(size_t(d.H) * 4); h.off_dq = take(thd);
+    h.off_dkv = take(size_t(d.num_kv) * kD * 2); h.off_dsink = take(size_t(d.H) * 4);
+    h.bytes = off;
+    return h;
+}
 }  // namespace
 }  // namespace smla
 
@@ -219,6 +372,7 @@ int smla_workspace_size(int op, const smla_dims* dims, size_t* bytes) {
     if (rc) return rc;
     if (op == SMLA_OP_FWD) { *bytes = kStatusBytes; return SMLA_OK; }
     if (op == SMLA_OP_BWD) { *bytes = plan_bwd(*dims).bytes; return SMLA_OK; }
+    if (op == SMLA_OP_BWD_HOST) { *bytes = plan_host(*dims, plan_bwd(*dims)).bytes; return SMLA_OK; }
     return SMLA_ERR_ARG;
 }
 
@@ -277,73 +431,107 @@ int smla_bwd(const uint16_t* q, const uint16_t* kv, const uint16_t* dO, const ui
     if ((rc = check_overlap(outs, 4, ins, 7))) return rc;
     if ((rc = check_arch())) return rc;
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    char* ws = static_cast<char*>(workspace);
-    unsigned* status = reinterpret_cast<unsigned*>(ws);
-    if ((rc = cuda_rc(cudaMemsetAsync(status, 0, sizeof(unsigned), s)))) return rc;
-    if (d.T == 0) {
-        if ((rc = cuda_rc(cudaMemsetAsync(dkv, 0, size_t(d.num_kv) * kD * 2, s)))) return rc;
-        if (d_sink) return cuda_rc(cudaMemsetAsync(d_sink, 0, size_t(d.H) * 4, s));
-        return SMLA_OK;
-    }
-    float* delta = reinterpret_cast<float*>(ws + plan.off_delta);
-    int32_t* row_ptr = reinterpret_cast<int32_t*>(ws + plan.off_rowptr);
-    int32_t* col = reinterpret_cast<int32_t*>(ws + plan.off_col);
-    uint16_t* interm = reinterpret_cast<uint16_t*>(ws + plan.off_interm);
-    uint16_t* dsT = reinterpret_cast<uint16_t*>(ws + plan.off_dst);
-    float* dq_acc = plan.nchunks > 1 ? reinterpret_cast<float*>(ws + plan.off_dqacc) : nullptr;
-    float* dkv_acc = plan.nchunks > 1 ? reinterpret_cast<float*>(ws + plan.off_dkvacc) : nullptr;
+    const BwdArgs A{q, kv, dO, o, lse, topk, sink, dq, dkv, d_sink};
+    return enqueue_bwd(A, d, plan, static_cast<char*>(workspace), static_cast<cudaStream_t>(stream),
+                       nullptr);
+}
 
-    SideStream* side = side_stream();
-    if (!side) return SMLA_ERR_CUDA;
-    const float scale = eff_scale(d);
-    for (int c = 0; c < plan.nchunks; ++c) {
-        const int r0 = int(c * plan.R);
-        const bool first = c == 0, last = c == plan.nchunks - 1;
-        // CSR of this chunk on the side stream (after the previous chunk's gather,
-        // which read the CSR buffers); joined back before this chunk's gather
-        if ((rc = cuda_rc(cudaEventRecord(side->fork, s)))) return rc;
-        if ((rc = cuda_rc(cudaStreamWaitEvent(side->stream, side->fork, 0)))) return rc;
-        {
-            prof::Scope ph(prof::kCsr, side->stream);
-            rc = cuda_rc(launch_csr(topk, d.T, d.topk, r0, int(plan.R), d.num_kv, row_ptr, col,
-                                    ws + plan.off_csr, plan.csr, status, side->stream));
-            if (rc) return rc;
-        }
-        if ((rc = cuda_rc(cudaEventRecord(side->join, side->stream)))) return rc;
-        if (first) {
-            prof::Scope ph(prof::kDelta, s);
-            if ((rc = cuda_rc(launch_delta(o, dO, delta, int64_t(d.T) * d.H, s)))) return rc;
-        }
-        ChunkArgs a{};
-        a.q = q; a.kv = kv; a.dO = dO; a.lse = lse; a.delta = delta; a.topk = topk;
-        a.T = d.T; a.H = d.H; a.K = d.topk; a.N = d.num_kv; a.r0 = r0; a.R = int(plan.R);
-        a.scale = scale; a.interm = interm; a.dsT = dsT; a.dq_acc = dq_acc; a.dq_out = dq;
-        a.first_chunk = first; a.last_chunk = last; a.status = status;
-        {
-            prof::Scope ph(prof::kSdi, s);
-            if ((rc = cuda_rc(launch_attn_sdi(a, s)))) return rc;
-        }
-        {
-            prof::Scope ph(prof::kDq, s);
-            if ((rc = cuda_rc(launch_attn_dq(a, s)))) return rc;
-        }
-        if ((rc = cuda_rc(cudaStreamWaitEvent(s, side->join, 0)))) return rc;
-        prof::Scope ph(prof::kGather, s);
-        rc = cuda_rc(launch_gather(row_ptr, col, interm, d.num_kv, plan.max_segs,
-                                   reinterpret_cast<int32_t*>(ws + plan.off_segcnt),
-                                   reinterpret_cast<int32_t*>(ws + plan.off_segptr),
-                                   reinterpret_cast<int32_t*>(ws + plan.off_segrow),
-                                   ws + plan.off_scan_tmp2,
-                                   reinterpret_cast<float*>(ws + plan.off_partial), dkv_acc, dkv,
-                                   first, last, s));
-        if (rc) return rc;
+int smla_bwd_host(const uint16_t* q, const uint16_t* kv, const uint16_t* dO, const uint16_t* o,
+                  const float* lse, const int32_t* topk, const float* sink, uint16_t* dq,
+                  uint16_t* dkv, float* d_sink, const smla_dims* dims, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+    int rc = check_dims(dims, true);
+    if (rc) return rc;
+    const smla_dims& d = *dims;
+    const bool has_tokens = d.T > 0;
+    if (!kv || !dkv || !workspace) return SMLA_ERR_NULL;
+    if (has_tokens && (!q || !dO || !o || !lse || !topk || !dq)) return SMLA_ERR_NULL;
+    if ((sink == nullptr) != (d_sink == nullptr)) return SMLA_ERR_SINK;
+    if (!aligned16(workspace)) return SMLA_ERR_ALIGN;
+    const BwdPlan plan = plan_bwd(d);
+    const HostPlan hp = plan_host(d, plan);
+    if (workspace_bytes < hp.bytes) return SMLA_ERR_WORKSPACE;
+    const size_t thd = size_t(d.T) * d.H * kD * 2, th4 = size_t(d.T) * d.H * 4;
+    const size_t kvb = size_t(d.num_kv) * kD * 2, tkb = size_t(d.T) * d.topk * 4;
+    const size_t hb = sink ? size_t(d.H) * 4 : 0;
+    const Span ins[] = {{q, thd}, {kv, kvb}, {dO, thd}, {o, thd}, {lse, th4}, {topk, tkb}, {sink, hb}};
+    const Span outs[] = {{dq, thd}, {dkv, kvb}, {d_sink, hb}};
+    if ((rc = check_overlap(outs, 3, ins, 7))) return rc;
+    if ((rc = check_arch())) return rc;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    HostStreams* H = host_streams();
+    if (!H) return SMLA_ERR_CUDA;
+    char* ws = static_cast<char*>(workspace);
+    BwdArgs A{};
+    A.q = reinterpret_cast<uint16_t*>(ws + hp.off_q);
+    A.kv = reinterpret_cast<uint16_t*>(ws + hp.off_kv);
+    A.dO = reinterpret_cast<uint16_t*>(ws + hp.off_dO);
+    A.o = reinterpret_cast<uint16_t*>(ws + hp.off_o);
+    A.lse = reinterpret_cast<float*>(ws + hp.off_lse);
+    A.topk = reinterpret_cast<int32_t*>(ws + hp.off_topk);
+    A.sink = sink ? reinterpret_cast<float*>(ws + hp.off_sink) : nullptr;
+    A.dq = reinterpret_cast<uint16_t*>(ws + hp.off_dq);
+    A.dkv = reinterpret_cast<uint16_t*>(ws + hp.off_dkv);
+    A.d_sink = sink ? reinterpret_cast<float*>(ws + hp.off_dsink) : nullptr;
+    auto h2d = [&](const void* dst, const void* src, size_t n) {
+        return n ? cudaMemcpyAsync(const_cast<void*>(dst), src, n, cudaMemcpyHostToDevice, H->in)
+                 : cudaSuccess;
+    };
+    auto d2h = [&](void* dst, const void* src, size_t n) {
+        return n ? cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToHost, H->out) : cudaSuccess;
+    };
+    // the copy streams start after everything already queued on the caller's
+    // stream (earlier calls may still use this workspace)
+    if ((rc = cuda_rc(cudaEventRecord(H->fork, s)))) return rc;
+    if ((rc = cuda_rc(cudaStreamWaitEvent(H->in, H->fork, 0)))) return rc;
+    if ((rc = cuda_rc(cudaStreamWaitEvent(H->out, H->fork, 0)))) return rc;
+    // small inputs first: the CSR build needs only topk
+    if ((rc = cuda_rc(h2d(A.topk, topk, tkb)))) return rc;
+    if ((rc = cuda_rc(h2d(A.kv, kv, kvb)))) return rc;
+    if ((rc = cuda_rc(h2d(A.lse, lse, th4)))) return rc;
+    if ((rc = cuda_rc(h2d(A.sink, sink, hb)))) return rc;
+    if ((rc = cuda_rc(cudaEventRecord(H->small_in, H->in)))) return rc;
+    // then o, dO and q in token chunks of about 512 tokens
+    int nt = (d.T + 511) / 512;
+    if (nt < 1) nt = 1;
+    if (nt > kMaxTokenChunks) nt = kMaxTokenChunks;
+    int tb[kMaxTokenChunks + 1];
+    for (int i = 0; i <= nt; ++i) tb[i] = int(int64_t(d.T) * i / nt);
+    for (int i = 0; i < nt; ++i) {
+        const size_t b0 = size_t(tb[i]) * d.H * kD * 2, nb = size_t(tb[i + 1] - tb[i]) * d.H * kD * 2;
+        const char* ob = reinterpret_cast<const char*>(o);
+        const char* db = reinterpret_cast<const char*>(dO);
+        const char* qb = reinterpret_cast<const char*>(q);
+        if ((rc = cuda_rc(h2d(reinterpret_cast<const char*>(A.o) + b0, ob + b0, nb)))) return rc;
+        if ((rc = cuda_rc(h2d(reinterpret_cast<const char*>(A.dO) + b0, db + b0, nb)))) return rc;
+        if ((rc = cuda_rc(h2d(reinterpret_cast<const char*>(A.q) + b0, qb + b0, nb)))) return rc;
+        if ((rc = cuda_rc(cudaEventRecord(H->in_ready[i], H->in)))) return rc;
     }
-    if (sink) {
-        prof::Scope ph(prof::kDsink, s);
-        if ((rc = cuda_rc(launch_dsink(delta, lse, sink, d_sink, d.T, d.H, s)))) return rc;
+    if ((rc = cuda_rc(cudaStreamWaitEvent(s, H->small_in, 0)))) return rc;
+    const TokenFeed feed{nt, tb, H->in_ready, H->dq_ready};
+    if ((rc = enqueue_bwd(A, d, plan, ws, s, &feed))) return rc;
+    // results: dq per token chunk as soon as it is final, then dkv and d_sink
+    if (has_tokens) {
+        for (int i = 0; i < nt; ++i) {
+            if (tb[i + 1] <= tb[i]) continue;
+            const size_t b0 = size_t(tb[i]) * d.H * kD * 2, nb = size_t(tb[i + 1] - tb[i]) * d.H * kD * 2;
+            if ((rc = cuda_rc(cudaStreamWaitEvent(H->out, H->dq_ready[i], 0)))) return rc;
+            if ((rc = cuda_rc(d2h(reinterpret_cast<char*>(dq) + b0,
+                                  reinterpret_cast<const char*>(A.dq) + b0, nb)))) return rc;
+        }
+    } else {
+        // T == 0: wait for the input copies before the caller's stream goes on
+        if ((rc = cuda_rc(cudaStreamWaitEvent(s, H->in_ready[0], 0)))) return rc;
     }
-    return SMLA_OK;
+    if ((rc = cuda_rc(cudaEventRecord(H->done, s)))) return rc;
+    if ((rc = cuda_rc(cudaStreamWaitEvent(H->out, H->done, 0)))) return rc;
+    if ((rc = cuda_rc(d2h(dkv, A.dkv, kvb)))) return rc;
+    if ((rc = cuda_rc(d2h(d_sink, A.d_sink, hb)))) return rc;
+    // the caller's stream waits for the copies out, so that synchronizing it
+    // (or an event recorded on it) covers the whole call
+    if ((rc = cuda_rc(cudaEventRecord(H->out_done, H->out)))) return rc;
+    return cuda_rc(cudaStreamWaitEvent(s, H->out_done, 0));
 }
 
 int smla_csr_build(const int32_t* topk, int32_t T, int32_t topk_w, int32_t r0, int32_t r_len,

@@ -155,3 +155,47 @@ def test_fwd_validation(lib):
     d2 = SmlaDims(**{**BASE, "D": 128})
     assert f(a["q"], a["kv"], a["topk"], a["sink"], a["o"], a["lse"], ctypes.byref(d2),
              a["ws"], 4096, None) == _lib.SMLA_ERR_D512
+
+
+def _bwd_host(lib, dims, a, ws_bytes=None):
+    if ws_bytes is None:
+        n = ctypes.c_size_t()
+        rc = lib.smla_workspace_size(_lib.SMLA_OP_BWD_HOST, ctypes.byref(dims), ctypes.byref(n))
+        if rc:
+            return rc
+        ws_bytes = n.value
+    return lib.smla_bwd_host(a["q"], a["kv"], a["do"], a["o"], a["lse"], a["topk"], a["sink"],
+                             a["dq"], a["dkv"], a["dsink"], ctypes.byref(dims), a["ws"], ws_bytes,
+                             None)
+
+
+def test_bwd_host_workspace_holds_device_copies(lib):
+    d = SmlaDims(**{**BASE, "T": 4096, "H": 128, "topk": 512, "num_kv": 5120})
+    n_dev, n_host = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.smla_workspace_size(_lib.SMLA_OP_BWD, ctypes.byref(d), ctypes.byref(n_dev)) == 0
+    assert lib.smla_workspace_size(_lib.SMLA_OP_BWD_HOST, ctypes.byref(d), ctypes.byref(n_host)) == 0
+    # q, dO, o and dq (4 x 512 MiB) plus kv, dkv, lse, topk and sink live in the workspace
+    copies = 4 * 4096 * 128 * 512 * 2 + 2 * 5120 * 512 * 2 + 4096 * 128 * 4 + 4096 * 512 * 4
+    assert n_host.value >= n_dev.value + copies
+
+
+def test_bwd_host_validation(lib):
+    dims = SmlaDims(**BASE)
+    a = _addrs(); a["q"] = None
+    assert _bwd_host(lib, dims, a) == _lib.SMLA_ERR_NULL
+    a = _addrs(); a["dsink"] = None
+    assert _bwd_host(lib, dims, a) == _lib.SMLA_ERR_SINK
+    a = _addrs(); a["ws"] = ctypes.c_void_p(a["ws"].value + 8)
+    assert _bwd_host(lib, dims, a) == _lib.SMLA_ERR_ALIGN
+    a = _addrs(); a["dq"] = a["o"]
+    assert _bwd_host(lib, dims, a) == _lib.SMLA_ERR_OVERLAP
+    a = _addrs()
+    assert _bwd_host(lib, dims, a, ws_bytes=4096) == _lib.SMLA_ERR_WORKSPACE
+    assert _bwd_host(lib, SmlaDims(**{**BASE, "D": 128}), _addrs()) == _lib.SMLA_ERR_D512
+    # host pointers need no 16-byte alignment: with a valid call the only check
+    # left is the device's (the fake pointers must never reach a real copy)
+    import torch
+    if torch.cuda.is_available():
+        return
+    a = _addrs(); a["lse"] = ctypes.c_void_p(a["lse"].value + 4)
+    assert _bwd_host(lib, dims, a) in (_lib.SMLA_ERR_CUDA, _lib.SMLA_ERR_ARCH)
