@@ -384,11 +384,11 @@ OVERLAPPED_PHASES = ("csr",)
 # DRAM traffic per launch of the dominant kernels, from one ncu capture (see
 # profiles/), valid only while the kernel source is the one captured.
 _NCU_TRAFFIC = {
-    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "e0bf907c7a4a359a"),
-                 "bytes_per_token": (141.358848e6 + 290.918144e6) / 512,
+    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "29d339ceda10a603"),
+                 "bytes_per_token": (140.603136e6 + 274.493952e6) / 512,
                  "note": "ncu capture of the first 512 tokens, scaled by tokens"},
-    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "e0bf907c7a4a359a"),
-                "bytes_per_token": (69.777152e6 + 16.956672e6) / 512,
+    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "29d339ceda10a603"),
+                "bytes_per_token": (69.773056e6 + 16.423424e6) / 512,
                 "note": "ncu capture of the first 512 tokens, scaled by tokens"},
 }
 
@@ -418,8 +418,6 @@ def _algorithmic(phase: str, spec, topk):
         return {"bound": "tensor", "flops": 4 * 2 * 512 * H * valid / nchunks}
     if phase == "attn_dq":
         return {"bound": "tensor", "flops": 1 * 2 * 512 * H * valid / nchunks}
-    if phase == "attn":           # CUDA-core path: all five products on FMA units
-        return {"bound": "alu", "flops": 5 * 2 * 512 * H * valid / nchunks}
     if phase == "delta":
         return {"bound": "hbm", "bytes": 2 * T * H * 512 * 2 + T * H * 4}
     if phase == "gather":

@@ -17,13 +17,16 @@
  *
  * Conventions (all entry points):
  *   - Every tensor is a row-major, contiguous DEVICE buffer owned by the
- *     caller: q, dO, o, dq are [T, H, D]; kv, dkv are [num_kv, D]; lse is
- *     [T, H]; topk is [T, topk]; sink, d_sink are [H].
- *     bf16 tensors are passed as uint16_t bit patterns.
+ *     caller (HOST buffers for smla_bwd_host): q, dO, o, dq are [T, H, D];
+ *     kv, dkv are [num_kv, D]; lse is [T, H]; topk is [T, topk]; sink, d_sink
+ *     are [H]. bf16 tensors are passed as uint16_t bit patterns.
  *   - Every device pointer must be 16-byte aligned.
- *   - The library allocates nothing during a call. The caller passes a device
- *     workspace of at least smla_workspace_size() bytes. The library keeps no
- *     state between calls except a per-device cache of the arch check.
+ *   - The library allocates no device memory during a call. The caller passes
+ *     a device workspace of at least smla_workspace_size() bytes. Between calls
+ *     the library keeps a per-device cache of the arch check and, per host
+ *     thread and device, the streams and events it creates on first use: a
+ *     side stream on which smla_bwd builds the CSR (forked from and joined back
+ *     into `stream` with events) and the two copy streams of smla_bwd_host.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and runs asynchronously. A returned SMLA_OK means the work was
  *     launched, not that it finished.

@@ -2,11 +2,12 @@
 times (same shapes, same rank chunking), on outputs the fp64 oracle can
 compute one by one:
 
-* dq for a sample of tokens (the first and last tokens, the end of the short
-  windows, and seeded random tokens);
-* dkv for a sample of kv rows (window rows, pool rows, and the rows with the
-  most contributors -- the hottest Zipf rows in the skewed workload), each
-  computed by the oracle from its full contributor list;
+* dq for at least 256 sampled tokens (the first and last tokens, the end of
+  the short windows, and seeded random tokens);
+* dkv for at least 64 sampled kv rows (window rows, pool rows, rows no token
+  selects, and the rows with the most contributors -- the hottest Zipf rows in
+  the skewed workload), each computed by the oracle from its full
+  contributor list;
 * all of d_sink;
 plus bitwise run-to-run determinism of dq, dkv and d_sink.
 
@@ -34,21 +35,33 @@ def _built():
     assert torch.cuda.is_available()
 
 
-def _sample_tokens(T, rng, n=40):
+def _sample_tokens(T, rng, n=256):
+    # at least 256 tokens: the first and last tokens, the end of the short
+    # windows, and seeded random tokens
     fixed = [0, 1, 2, 63, 126, 127, 128, T // 2, T - 2, T - 1]
-    rest = rng.choice(T, size=n - len(fixed), replace=False)
-    return np.unique(np.concatenate([fixed, rest]).astype(np.int64))
+    toks = set(fixed)
+    for t in rng.permutation(T):
+        if len(toks) >= n:
+            break
+        toks.add(int(t))
+    return np.array(sorted(toks), dtype=np.int64)
 
 
-def _sample_rows(topk, N, T, rng, n=32):
+def _sample_rows(topk, N, T, rng, n=64):
+    # at least 64 kv rows: the hottest rows, window rows, pool rows, rows no
+    # token selects, and the first / last rows
     counts = np.bincount(topk[topk >= 0], minlength=N)
-    hottest = np.argsort(-counts, kind="stable")[:6]
-    window = rng.choice(T, size=8, replace=False)
-    pool = T + rng.choice(N - T, size=8, replace=False) if N > T else np.array([], np.int64)
+    hottest = np.argsort(-counts, kind="stable")[:16]
+    window = rng.choice(T, size=20, replace=False)
+    pool = T + rng.choice(N - T, size=24, replace=False) if N > T else np.array([], np.int64)
     unused = np.flatnonzero(counts == 0)[:2]
     fixed = [0, T - 1, N - 1]
-    rows = np.concatenate([hottest, window, pool, unused, fixed]).astype(np.int64)
-    return np.unique(rows)
+    rows = set(np.concatenate([hottest, window, pool, unused, fixed]).astype(np.int64).tolist())
+    for j in rng.permutation(N):
+        if len(rows) >= n:
+            break
+        rows.add(int(j))
+    return np.array(sorted(rows), dtype=np.int64)
 
 
 @pytest.mark.parametrize("name", ["headline", "headline_h64_chunked", "t8192_zipf"])
