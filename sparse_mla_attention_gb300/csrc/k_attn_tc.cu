@@ -314,16 +314,17 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 const int pr = item % p.npairs;
                 const int ntiles = pr == p.npairs - 1 ? p.tiles_last : 2;
                 // A stage may overwrite TMEM only after the previous item's B stage
-                // read P / dS, and (when S^T | dP^T reach column 128) after its drains.
+                // read P / dS ...
                 if (it > 0) {
                     ok = ok && wait_or_abort(&sh.b_done[0], (it - 1) & 1, &sh.abort_flag, p.status);
                     ok = ok && wait_or_abort(&sh.b_done[1], (it - 1) & 1, &sh.abort_flag, p.status);
-                    if (2 * H > 128)
-                        for (int g = 0; g < 2 && ok; ++g)
-                            while (ok && xe_done[g] < x_uses[g]) {
-                                ok = wait_or_abort(&sh.x_empty[g], xe_done[g] & 1u, &sh.abort_flag, p.status);
-                                ++xe_done[g];
-                            }
+                    // ... and after its drains, which follow the dS stash (the stash
+                    // reads P^T / dS^T columns that this A stage overwrites)
+                    for (int g = 0; g < 2 && ok; ++g)
+                        while (ok && xe_done[g] < x_uses[g]) {
+                            ok = wait_or_abort(&sh.x_empty[g], xe_done[g] & 1u, &sh.abort_flag, p.status);
+                            ++xe_done[g];
+                        }
                 }
                 SMLA_TRACE_EV(0, it, 3);
                 for (int c = 0; c < 8 && ok; ++c) {
@@ -492,6 +493,19 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 tmem_wait_st();
                 if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 12);
                 if (warp == 9 && lane == 0) SMLA_TRACE_EV(0, it, 62);
+            }
+            if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 13);
+            if (warp == 9 && lane == 0) SMLA_TRACE_EV(0, it, 63);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.p_ready);
+            if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 8);
+            if (active) {
+                // P^T and dS^T are read by the B-stage MMAs from here on (read only);
+                // the stash reads dS^T alongside them. The next item's A stage
+                // overwrites these columns only after this warp's drains below.
+                __syncwarp();               // tcgen05.ld is warp-collective
+                const uint32_t trow = tbase + lane_off + g * 256;
                 // stash scale * dS^T for the dq kernel: per 64-head block the warp's 32
                 // rows are read back from TMEM, go through the staging tile and leave
                 // in one TMA store (heads >= H are 0)
@@ -523,12 +537,6 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     __syncwarp();
                 }
             }
-            if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 13);
-            if (warp == 9 && lane == 0) SMLA_TRACE_EV(0, it, 63);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.p_ready);
-            if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 8);
             // drain interm columns [128c, 128c + 128) of this warp's tile, in halves
             bool ok = true;
             for (int c = 0; c < 4 && active; ++c) {
