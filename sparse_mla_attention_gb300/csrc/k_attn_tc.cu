@@ -148,6 +148,7 @@ struct SdiCfg {
     static constexpr uint32_t kIdescB = idesc_bf16(128, 128, false, true);
     static constexpr int kUses = 12;        // ring uses per item: 8 A-stage + 4 B-stage
     static_assert(kSlots >= 3, "the copy pipeline needs at least three slots");
+    static_assert(kSmem <= 232448, "shared memory of one CTA is at most 227 KB");
 };
 
 template <int H>
@@ -621,14 +622,21 @@ struct DqShared {
 };
 
 constexpr int kDqSlots = 4;
+// Copy warps: many warps with few copies each in flight gather faster than a
+// few warps with many (a warp's issue stalls once it has many cp.async
+// operations outstanding).
+constexpr int kDqCopyWarps = 16;
+constexpr int kDqRowsPerWarp = 64 / kDqCopyWarps;           // rows of a 64-rank chunk
+constexpr int kDqThreads = (6 + kDqCopyWarps) * 32;         // TMA, MMA, 4 epilogue, copy warps
 constexpr int kDqABytes = 2 * 64 * 128;        // two 64-head blocks x 64 ranks
 constexpr int kDqBBytes = 4 * 64 * 128;        // four 64-column blocks x 64 ranks
 constexpr int kDqSlotBytes = kDqABytes + kDqBBytes;
 constexpr int kDqSmem = int(sizeof(DqShared)) + 1024 + kDqSlots * kDqSlotBytes;
+static_assert(kDqSmem <= 232448, "shared memory of one CTA is at most 227 KB");
 constexpr uint32_t kDqIdesc = idesc_bf16(128, 256, true, true);
 
 template <int H>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
 dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
     extern __shared__ uint8_t smem_raw[];
     DqShared& sh = *reinterpret_cast<DqShared*>(smem_raw);
@@ -638,8 +646,11 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
     const int nkc = p.Rp / 64;
 
     if (threadIdx.x == 0) {
-        // full: the TMA thread's arrive (with the dS bytes) + 128 copy threads
-        for (int s = 0; s < kDqSlots; ++s) { mbar_init(&sh.full[s], 129); mbar_init(&sh.empty[s], 1); }
+        // full: the TMA thread's arrive (with the dS bytes) + every copy thread
+        for (int s = 0; s < kDqSlots; ++s) {
+            mbar_init(&sh.full[s], 1 + 32 * kDqCopyWarps);
+            mbar_init(&sh.empty[s], 1);
+        }
         for (int b = 0; b < 2; ++b) { mbar_init(&sh.d_full[b], 1); mbar_init(&sh.d_empty[b], 4); }
         mbar_init(&sh.drain, 1);
         sh.abort_flag = 0;
@@ -683,11 +694,12 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
         __syncwarp();
     } else if (warp >= 6) {
         // ------------------------------------------------ kv gather (cp.async)
-        // Per 64-rank chunk, copy warp gw copies rows 16gw .. 16gw + 15, one row
-        // per round: lane l copies the 16-byte piece (l & 7) of 64-column block
-        // (l >> 3) of the row's half of D. Lane i < 16 holds the index of row
-        // 16gw + i; indices are loaded two chunks ahead over this CTA's whole
-        // chunk sequence, and pending copies carry over from item to item.
+        // Per 64-rank chunk, copy warp gw copies rows R*gw .. R*gw + R - 1
+        // (R = kDqRowsPerWarp), one row per round: lane l copies the 16-byte piece
+        // (l & 7) of 64-column block (l >> 3) of the row's half of D. The row
+        // indices come in batches of 32 / R chunks, loaded one batch ahead: lane l
+        // holds row R*gw + (l % R) of chunk (l / R) of the batch.
+        constexpr int kR = kDqRowsPerWarp, kBatch = 32 / kR;
         const int gw = warp - 6;
         const int db = lane >> 3, piece = lane & 7;
         int slot = 0; uint32_t phase = 0;
@@ -695,10 +707,11 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
         const int my_items =
             int(blockIdx.x) < nitems ? (nitems - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
         const int nchunks = my_items * nkc;
-        auto load_idx = [&](int n) -> int {
+        auto batch_idx = [&](int b) -> int {   // this lane's index in batch b
+            const int n = b * kBatch + lane / kR;
             if (n >= nchunks) return 0;
             const int item = blockIdx.x + (n / nkc) * int(gridDim.x);
-            const int rl = (n % nkc) * 64 + 16 * gw + (lane & 15);
+            const int rl = (n % nkc) * 64 + kR * gw + lane % kR;
             int j = 0;
             if (rl < p.R) {
                 j = __ldg(p.topk + int64_t(item >> 1) * p.K + p.r0 + rl);
@@ -706,7 +719,7 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
             }
             return j;
         };
-        int i0 = load_idx(0), i1 = load_idx(1);
+        int cur = batch_idx(0), nxt = batch_idx(1);
         int pend[kDqSlots] = {0, 0, 0, 0};
         int npend = 0;
         auto flush_one = [&]() {
@@ -716,27 +729,31 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
             for (int k = 0; k + 1 < kDqSlots; ++k) pend[k] = pend[k + 1];
             --npend;
         };
-        for (int n = 0; n < nchunks && ok; ++n) {
-            const int item = blockIdx.x + (n / nkc) * int(gridDim.x);
-            const int i2 = load_idx(n + 2);
-            if (lane == 0) ok = wait_or_abort(&sh.empty[slot], phase ^ 1u, &sh.abort_flag, p.status);
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (!ok) break;
-            const char* src0 =
-                reinterpret_cast<const char*>(p.kv) + ((item & 1) * 256 + db * 64) * 2 + piece * 16;
-            uint8_t* bt = slots + slot * kDqSlotBytes + kDqABytes + db * 8192;
+        for (int b = 0; b * kBatch < nchunks && ok; ++b) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int r = 16 * gw + i;
-                const int j = __shfl_sync(0xffffffffu, i0, i);
-                cp_async16(bt + r * 128 + ((piece ^ (r & 7)) << 4), src0 + int64_t(j) * (kD * 2));
+            for (int u = 0; u < kBatch; ++u) {
+                const int n = b * kBatch + u;
+                if (n >= nchunks) break;
+                const int item = blockIdx.x + (n / nkc) * int(gridDim.x);
+                if (lane == 0) ok = wait_or_abort(&sh.empty[slot], phase ^ 1u, &sh.abort_flag, p.status);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                const char* src0 =
+                    reinterpret_cast<const char*>(p.kv) + ((item & 1) * 256 + db * 64) * 2 + piece * 16;
+                uint8_t* bt = slots + slot * kDqSlotBytes + kDqABytes + db * 8192;
+#pragma unroll
+                for (int i = 0; i < kR; ++i) {
+                    const int r = kR * gw + i;
+                    const int j = __shfl_sync(0xffffffffu, cur, u * kR + i);
+                    cp_async16(bt + r * 128 + ((piece ^ (r & 7)) << 4), src0 + int64_t(j) * (kD * 2));
+                }
+                cp_async_commit();
+                pend[npend++] = slot;
+                if (npend == kDqSlots - 1) { cp_async_wait<kDqSlots - 2>(); flush_one(); }
+                advance(slot, phase, kDqSlots);
             }
-            cp_async_commit();
-            pend[npend++] = slot;
-            if (npend == kDqSlots - 1) { cp_async_wait<kDqSlots - 2>(); flush_one(); }
-            advance(slot, phase, kDqSlots);
-            i0 = i1;
-            i1 = i2;
+            cur = nxt;
+            nxt = batch_idx(b + 2);
         }
         cp_async_wait<0>();
         while (npend > 0) flush_one();
@@ -903,7 +920,7 @@ cudaError_t launch_dq_h(const ChunkArgs& a, cudaStream_t s) {
     const int64_t items = int64_t(a.T) * 2;
     const int sms = sm_count();
     const int grid = int(items < sms ? items : sms);
-    dq_kernel<H><<<grid, 320, kDqSmem, s>>>(mds, dp);
+    dq_kernel<H><<<grid, kDqThreads, kDqSmem, s>>>(mds, dp);
     note_launch();
     return cudaGetLastError();
 }
