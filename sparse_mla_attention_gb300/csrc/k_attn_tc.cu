@@ -622,11 +622,11 @@ struct DqShared {
 };
 
 constexpr int kDqSlots = 4;
-// Copy warps: many warps with few copies each in flight gather faster than a
-// few warps with many (a warp's issue stalls once it has many cp.async
-// operations outstanding).
-constexpr int kDqCopyWarps = 16;
-constexpr int kDqRowsPerWarp = 64 / kDqCopyWarps;           // rows of a 64-rank chunk
+// Copy warps: one team of 4 warps per ring slot. Team k fills slot k with the
+// chunks k, k + 4, ... (16 rows per warp), waits for its own copies only and
+// signals the slot, so four chunks are in flight, one per team.
+constexpr int kDqTeamWarps = 4;
+constexpr int kDqCopyWarps = kDqSlots * kDqTeamWarps;
 constexpr int kDqThreads = (6 + kDqCopyWarps) * 32;         // TMA, MMA, 4 epilogue, copy warps
 constexpr int kDqABytes = 2 * 64 * 128;        // two 64-head blocks x 64 ranks
 constexpr int kDqBBytes = 4 * 64 * 128;        // four 64-column blocks x 64 ranks
@@ -646,9 +646,9 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
     const int nkc = p.Rp / 64;
 
     if (threadIdx.x == 0) {
-        // full: the TMA thread's arrive (with the dS bytes) + every copy thread
+        // full: the TMA thread's arrive (with the dS bytes) + the 128 threads of the slot's team
         for (int s = 0; s < kDqSlots; ++s) {
-            mbar_init(&sh.full[s], 1 + 32 * kDqCopyWarps);
+            mbar_init(&sh.full[s], 1 + 32 * kDqTeamWarps);  // TMA thread + the slot's team
             mbar_init(&sh.empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) { mbar_init(&sh.d_full[b], 1); mbar_init(&sh.d_empty[b], 4); }
@@ -694,24 +694,21 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
         __syncwarp();
     } else if (warp >= 6) {
         // ------------------------------------------------ kv gather (cp.async)
-        // Per 64-rank chunk, copy warp gw copies rows R*gw .. R*gw + R - 1
-        // (R = kDqRowsPerWarp), one row per round: lane l copies the 16-byte piece
-        // (l & 7) of 64-column block (l >> 3) of the row's half of D. The row
-        // indices come in batches of 32 / R chunks, loaded one batch ahead: lane l
-        // holds row R*gw + (l % R) of chunk (l / R) of the batch.
-        constexpr int kR = kDqRowsPerWarp, kBatch = 32 / kR;
+        // Team k (warps 4k .. 4k + 3 of the copy warps) fills ring slot k with the
+        // chunks n = k, k + 4, ... of this CTA's chunk sequence; warp w of the team
+        // copies rows 16w .. 16w + 15, one row per round: lane l copies the 16-byte
+        // piece (l & 7) of 64-column block (l >> 3) of the row's half of D. Lane
+        // i < 16 holds the index of row 16w + i, loaded one chunk of the team ahead.
         const int gw = warp - 6;
+        const int team = gw / kDqTeamWarps, wt = gw % kDqTeamWarps;
         const int db = lane >> 3, piece = lane & 7;
-        int slot = 0; uint32_t phase = 0;
-        bool ok = true;
         const int my_items =
             int(blockIdx.x) < nitems ? (nitems - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
         const int nchunks = my_items * nkc;
-        auto batch_idx = [&](int b) -> int {   // this lane's index in batch b
-            const int n = b * kBatch + lane / kR;
+        auto load_idx = [&](int n) -> int {
             if (n >= nchunks) return 0;
             const int item = blockIdx.x + (n / nkc) * int(gridDim.x);
-            const int rl = (n % nkc) * 64 + kR * gw + lane % kR;
+            const int rl = (n % nkc) * 64 + 16 * wt + (lane & 15);
             int j = 0;
             if (rl < p.R) {
                 j = __ldg(p.topk + int64_t(item >> 1) * p.K + p.r0 + rl);
@@ -719,44 +716,33 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
             }
             return j;
         };
-        int cur = batch_idx(0), nxt = batch_idx(1);
-        int pend[kDqSlots] = {0, 0, 0, 0};
-        int npend = 0;
-        auto flush_one = [&]() {
-            fence_proxy_async_smem();
-            mbar_arrive(&sh.full[pend[0]]);
+        int idx = load_idx(team);
+        uint32_t phase = 0;
+        uint8_t* sbase = slots + team * kDqSlotBytes + kDqABytes;
+        for (int n = team; n < nchunks; n += kDqSlots) {
+            const int item = blockIdx.x + (n / nkc) * int(gridDim.x);
+            bool ok = true;
+            if (lane == 0) ok = wait_or_abort(&sh.empty[team], phase ^ 1u, &sh.abort_flag, p.status);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            const int nxt = load_idx(n + kDqSlots);
+            const char* src0 =
+                reinterpret_cast<const char*>(p.kv) + ((item & 1) * 256 + db * 64) * 2 + piece * 16;
+            uint8_t* bt = sbase + db * 8192;
 #pragma unroll
-            for (int k = 0; k + 1 < kDqSlots; ++k) pend[k] = pend[k + 1];
-            --npend;
-        };
-        for (int b = 0; b * kBatch < nchunks && ok; ++b) {
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int n = b * kBatch + u;
-                if (n >= nchunks) break;
-                const int item = blockIdx.x + (n / nkc) * int(gridDim.x);
-                if (lane == 0) ok = wait_or_abort(&sh.empty[slot], phase ^ 1u, &sh.abort_flag, p.status);
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                if (!ok) break;
-                const char* src0 =
-                    reinterpret_cast<const char*>(p.kv) + ((item & 1) * 256 + db * 64) * 2 + piece * 16;
-                uint8_t* bt = slots + slot * kDqSlotBytes + kDqABytes + db * 8192;
-#pragma unroll
-                for (int i = 0; i < kR; ++i) {
-                    const int r = kR * gw + i;
-                    const int j = __shfl_sync(0xffffffffu, cur, u * kR + i);
-                    cp_async16(bt + r * 128 + ((piece ^ (r & 7)) << 4), src0 + int64_t(j) * (kD * 2));
-                }
-                cp_async_commit();
-                pend[npend++] = slot;
-                if (npend == kDqSlots - 1) { cp_async_wait<kDqSlots - 2>(); flush_one(); }
-                advance(slot, phase, kDqSlots);
+            for (int i = 0; i < 16; ++i) {
+                const int r = 16 * wt + i;
+                const int j = __shfl_sync(0xffffffffu, idx, i);
+                cp_async16(bt + r * 128 + ((piece ^ (r & 7)) << 4), src0 + int64_t(j) * (kD * 2));
             }
-            cur = nxt;
-            nxt = batch_idx(b + 2);
+            cp_async_commit();
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            mbar_arrive(&sh.full[team]);
+            phase ^= 1u;
+            idx = nxt;
         }
         cp_async_wait<0>();
-        while (npend > 0) flush_one();
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
