@@ -384,11 +384,11 @@ OVERLAPPED_PHASES = ("csr",)
 # DRAM traffic per launch of the dominant kernels, from one ncu capture (see
 # profiles/), valid only while the kernel source is the one captured.
 _NCU_TRAFFIC = {
-    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "29d339ceda10a603"),
-                 "bytes_per_token": (140.603136e6 + 274.493952e6) / 512,
+    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "56bdc8853f47ed95"),
+                 "bytes_per_token": (141.410048e6 + 274.877696e6) / 512,
                  "note": "ncu capture of the first 512 tokens, scaled by tokens"},
-    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "29d339ceda10a603"),
-                "bytes_per_token": (69.773056e6 + 16.423424e6) / 512,
+    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "56bdc8853f47ed95"),
+                "bytes_per_token": (69.759232e6 + 16.248320e6) / 512,
                 "note": "ncu capture of the first 512 tokens, scaled by tokens"},
 }
 
