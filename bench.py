@@ -6,7 +6,8 @@ dq, atomic-free dKV gather, d_sink) through the C ABI on the headline
 workload of the aiter page's Performance table: T=4096, H=128, D=512,
 topk=512, num_kv=5120 (128-row causal window + 384 uniform pool picks),
 synthetic seeded inputs (no dataset exists for it). O and lse come from the
-library's forward (untimed).
+library's forward, which is also timed on its own and reported under
+"forward" (not part of the step).
 
 Prints ONE JSON line (rank 0). The metric is TFLOPS over the valid
 (token, head, rank) triples at 5 GEMMs x 2 x 512 FLOPs each; ms/call is
@@ -347,6 +348,40 @@ def run_ours(args):
     roofline["traffic_note"] = tnote
     roofline["per_launch_ms"] = per_launch_ms
 
+    # ---- the forward (O, lse) on the same inputs, timed on its own; not part of the step
+    fwd = None
+    if not args.no_fwd:
+        f_o = torch.empty_like(q)
+        f_lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+        ws_f = smla.Workspace(dev)
+
+        def fwd_step():
+            smla.sparse_mla_fwd(q, kv, topk, sink, scale=inp["scale"], workspace=ws_f,
+                                check_status=False, out=(f_o, f_lse))
+
+        for _ in range(max(3, args.warmup)):
+            fwd_step()
+        if smla.device_status(ws_f.buf) != 0:
+            raise RuntimeError("device status set by the forward")
+        torch.cuda.synchronize(dev)
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            fwd_step()
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_f = f0.elapsed_time(f1) / args.steps
+        f_flops = 2 * 2 * 512 * H * W.valid_ranks(inp["topk"])   # S and O GEMMs
+        f_tf = f_flops / (ms_f * 1e-3) / 1e12
+        tc = H % 32 == 0 and 1 <= K <= 512
+        fwd = {"ms_per_call": ms_f, "tflops_valid": f_tf, "calls": args.steps,
+               "kernel": "fwd_tc_kernel" if tc else "fwd_kernel",
+               "roofline": {"bound": "tensor", "achieved": f_tf, "peak": peaks["bf16_tflops"],
+                            "unit": "TFLOP/s", "frac": f_tf / peaks["bf16_tflops"],
+                            "peak_source": peaks["source"] + " bf16 burst"},
+               "flops_valid_per_call": f_flops}
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_oracle_sample(spec, inp, seconds=args.cpu_seconds)
@@ -367,6 +402,7 @@ def run_ours(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "forward": fwd,
         "gpu_launches": launches,
         "clocks": clk,
         "pages_context": PAGES_CONTEXT,
@@ -438,6 +474,7 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fwd", action="store_true", help="skip the separate forward timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--tokens", type=int, default=0,
                     help="time only the first N tokens of the workload (small profiling cases)")

@@ -80,9 +80,12 @@ def device_status(workspace: torch.Tensor) -> int:
 
 def sparse_mla_fwd(q: torch.Tensor, kv: torch.Tensor, topk: torch.Tensor,
                    sink: Optional[torch.Tensor] = None, scale: Optional[float] = None,
-                   workspace: Optional[Workspace] = None, check_status: bool = True
+                   workspace: Optional[Workspace] = None, check_status: bool = True,
+                   out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None
                    ) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Forward: (o [T,H,512] bf16, lse [T,H] fp32, sink-inclusive, natural log)."""
+    """Forward: (o [T,H,512] bf16, lse [T,H] fp32, sink-inclusive, natural log).
+
+    `out` = (o, lse) writes into caller-owned tensors of those shapes."""
     _need(q, "q", torch.bfloat16, 3)
     _need(kv, "kv", torch.bfloat16, 2)
     _need(topk, "topk", torch.int32, 2)
@@ -95,8 +98,15 @@ def sparse_mla_fwd(q: torch.Tensor, kv: torch.Tensor, topk: torch.Tensor,
         raise ValueError("shape mismatch between q, kv and topk")
     dims = make_dims(T, H, topk.shape[1], kv.shape[0], 0, scale, D)
     ws = (workspace or Workspace(q.device)).get(workspace_size(SMLA_OP_FWD, dims))
-    o = torch.empty_like(q)
-    lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    if out is None:
+        o = torch.empty_like(q)
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = out
+        _need(o, "o", torch.bfloat16, 3)
+        _need(lse, "lse", torch.float32, 2)
+        if tuple(o.shape) != (T, H, D) or tuple(lse.shape) != (T, H):
+            raise ValueError("out must be (o [T,H,D], lse [T,H])")
     _lib.check(_lib.load().smla_fwd(_ptr(q), _ptr(kv), _ptr(topk), _ptr(sink), _ptr(o), _ptr(lse),
                                     ctypes.byref(dims), _ptr(ws), ws.numel(), _stream(q.device)),
                "smla_fwd")

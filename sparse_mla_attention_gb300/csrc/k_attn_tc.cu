@@ -97,6 +97,14 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
     return false;
 }
 
+// For warps that go on to warp-collective tcgen05 loads: every lane waits, and
+// the warp goes on only if all of them saw the phase.
+__device__ __forceinline__ bool wait_or_abort_warp(uint64_t* bar, uint32_t parity,
+                                                   volatile int* abort_flag, unsigned* status) {
+    const bool ok = wait_or_abort(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, ok) != 0;
+}
+
 __device__ __forceinline__ void advance(int& slot, uint32_t& phase, int nslots) {
     if (++slot == nslots) { slot = 0; phase ^= 1u; }
 }
@@ -407,7 +415,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         uint32_t x_use = 0;                             // accumulations of this tile consumed
         int it = 0;
         for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++it) {
-            if (sh.abort_flag) break;
+            if (__any_sync(0xffffffffu, sh.abort_flag != 0)) break;
             const int t = item / p.npairs, pr = item - t * p.npairs;
             const int ntiles = pr == p.npairs - 1 ? p.tiles_last : 2;
             const bool active = g < ntiles;
@@ -437,7 +445,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 if (h < H) { lsd[h] = lse_w[k]; lsd[H + h] = del_w[k]; }
             }
             __syncwarp();
-            if (!wait_or_abort(&sh.s_full, it & 1, &sh.abort_flag, p.status)) break;
+            if (!wait_or_abort_warp(&sh.s_full, it & 1, &sh.abort_flag, p.status)) break;
             if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 7);
             if (warp == 9 && lane == 0) SMLA_TRACE_EV(0, it, 44);
             __syncwarp();
@@ -541,7 +549,10 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             // drain interm columns [128c, 128c + 128) of this warp's tile, in halves
             bool ok = true;
             for (int c = 0; c < 4 && active; ++c) {
-                if (!wait_or_abort(&sh.x_full[g], x_use & 1u, &sh.abort_flag, p.status)) { ok = false; break; }
+                if (!wait_or_abort_warp(&sh.x_full[g], x_use & 1u, &sh.abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
                 ++x_use;
                 if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 32 + c);
                 __syncwarp();
@@ -785,7 +796,7 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
         for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++it) {
             const int t = item >> 1, half = item & 1;
             const int b = it & 1;
-            if (!wait_or_abort(&sh.d_full[b], (it >> 1) & 1, &sh.abort_flag, p.status)) break;
+            if (!wait_or_abort_warp(&sh.d_full[b], (it >> 1) & 1, &sh.abort_flag, p.status)) break;
             if (warp == 2 && lane == 0) SMLA_TRACE_EV(1, it, 4);
             __syncwarp();                   // tcgen05.ld is warp-collective
             tc_fence_after();

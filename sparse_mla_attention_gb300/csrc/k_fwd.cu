@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(kFwdHeads * 32) fwd_kernel(
 cudaError_t launch_fwd(const uint16_t* q, const uint16_t* kv, const int32_t* topk,
                        const float* sink, uint16_t* o, float* lse, int T, int H, int K,
                        int num_kv, float scale, unsigned* status, cudaStream_t s) {
+    const cudaError_t tc = launch_fwd_tc(q, kv, topk, sink, o, lse, T, H, K, num_kv, scale, status, s);
+    if (tc != cudaErrorNotSupported) return tc;
     if (T == 0) return cudaSuccess;
     dim3 grid(T, (H + kFwdHeads - 1) / kFwdHeads);
     fwd_kernel<<<grid, kFwdHeads * 32, 0, s>>>(

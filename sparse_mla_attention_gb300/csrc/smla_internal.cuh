@@ -112,6 +112,11 @@ cudaError_t launch_gather(const int32_t* row_ptr, const int32_t* col, const uint
 cudaError_t launch_fwd(const uint16_t* q, const uint16_t* kv, const int32_t* topk,
                        const float* sink, uint16_t* o, float* lse, int T, int H, int K,
                        int num_kv, float scale, unsigned* status, cudaStream_t s);
+// Tensor-core forward (H a multiple of 32 up to 128, 1 <= topk <= 512); returns
+// cudaErrorNotSupported for other shapes. launch_fwd tries it first.
+cudaError_t launch_fwd_tc(const uint16_t* q, const uint16_t* kv, const int32_t* topk,
+                          const float* sink, uint16_t* o, float* lse, int T, int H, int K,
+                          int num_kv, float scale, unsigned* status, cudaStream_t s);
 
 // Per-chunk attention backward core: for ranks [r0, r0+R) of each token, builds
 // interm [T, R, D] bf16 (sum_h P*dO + scale*dS*q) and dsT [T, R, H] bf16

@@ -102,6 +102,90 @@ def test_forward_no_sink_and_masked_rows():
     compare("o", to_f64(o), o64, cos_min=0.99999, rel=1e-2)
 
 
+# (H, K, N, T, sink): H a multiple of 32 with topk <= 512 runs on the tensor
+# cores, the other shapes on the CUDA-core kernel
+@pytest.mark.parametrize("H,K,N,T,sink", [
+    (32, 48, 90, 70, True),         # one ragged rank tile
+    (64, 200, 260, 130, False),     # two tiles, no sink
+    (96, 1, 20, 12, True),          # topk = 1
+    (128, 512, 700, 40, True),      # four full rank tiles
+    (128, 300, 520, 400, False),    # more tokens than SMs: the persistent loop
+    (64, 129, 300, 160, True),      # one rank past a tile boundary
+    (48, 80, 100, 30, True),        # H not a multiple of 32: CUDA-core kernel
+    (32, 600, 700, 20, True),       # topk > 512: CUDA-core kernel
+])
+def test_forward_shapes(H, K, N, T, sink):
+    c = custom_inputs(H * 11 + K, T=T, H=H, K=K, N=N, sink=sink,
+                      all_masked_rows=(min(2, T - 1),))
+    case = Case(c)
+    o_out = torch.full_like(case.q, float("nan"))
+    lse_out = torch.full((T, H), float("nan"), device="cuda")
+    o, lse = smla.sparse_mla_fwd(case.q, case.kv, case.topk, case.sink, scale=case.scale,
+                                 out=(o_out, lse_out))
+    o64, lse64 = oracle.fwd(case.q64, case.kv64, c["topk"], case.sink64, case.scale)
+    o_g, lse_g = to_f64(o), to_f64(lse)
+    m = min(2, T - 1)                       # the fully masked token
+    assert np.all(o_g[m] == 0)
+    if sink:
+        assert np.array_equal(lse_g[m], case.sink64)    # lse = sink exactly
+    else:
+        assert np.all(np.isneginf(lse_g[m]))
+    ok = np.isfinite(lse64)
+    assert np.array_equal(ok, np.isfinite(lse_g))
+    assert np.max(np.abs(lse_g[ok] - lse64[ok])) < 1e-4
+    compare("o", o_g, o64, cos_min=0.99999, rel=1e-2)
+
+
+def test_forward_after_backward_h32():
+    # The tensor-core forward runs M = 128 MMAs whatever H is; the TMEM lanes of
+    # heads >= H then hold scores of stale shared memory (the previous kernel's
+    # bytes). They must not change control flow: run the backward first so that
+    # shared memory holds its data, then the forward.
+    c = custom_inputs(91, T=300, H=32, K=256, N=400, sink=True, all_masked_rows=(7,))
+    case = Case(c)
+    for _ in range(2):
+        smla.sparse_mla_bwd(case.q, case.kv, case.do, case.o, case.lse, case.topk, case.sink,
+                            scale=case.scale)
+        o, lse = smla.sparse_mla_fwd(case.q, case.kv, case.topk, case.sink, scale=case.scale)
+        compare("o", to_f64(o), case.o64, cos_min=0.99999, rel=1e-2)
+        assert np.max(np.abs(to_f64(lse) - case.lse64)) < 1e-4
+
+
+def test_forward_t1024(t1024):
+    o1, lse1 = smla.sparse_mla_fwd(t1024.q, t1024.kv, t1024.topk, t1024.sink, scale=t1024.scale)
+    o2, lse2 = smla.sparse_mla_fwd(t1024.q, t1024.kv, t1024.topk, t1024.sink, scale=t1024.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(lse1, lse2)
+    # t1024.o64 / lse64: the oracle's forward rounded to bf16 / fp32
+    compare("o", to_f64(o1), t1024.o64, cos_min=0.99999, rel=1e-2)
+    assert np.max(np.abs(to_f64(lse1) - t1024.lse64)) < 1e-4
+
+
+@pytest.mark.parametrize("H", [16, 32])
+def test_forward_out_of_range_index_reports_and_masks(H):
+    c = custom_inputs(4, T=8, H=H, K=12, N=20, sink=True, mask_p=0.0)
+    case = Case(c)
+    bad = case.topk.clone()
+    bad[4, 5] = 20          # == num_kv: out of range
+    bad[6, 0] = -7
+    with pytest.raises(_lib.SmlaError) as e:
+        smla.sparse_mla_fwd(case.q, case.kv, bad, case.sink, scale=case.scale)
+    assert e.value.code == _lib.SMLA_ERR_INDEX
+    masked = bad.clone(); masked[4, 5] = -1; masked[6, 0] = -1
+    r1 = smla.sparse_mla_fwd(case.q, case.kv, bad, case.sink, scale=case.scale, check_status=False)
+    r2 = smla.sparse_mla_fwd(case.q, case.kv, masked, case.sink, scale=case.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(r1[0], r2[0]) and torch.equal(r1[1], r2[1])
+
+
+def test_forward_empty_T():
+    q = torch.zeros((0, 64, 512), dtype=torch.bfloat16, device="cuda")
+    kv = torch.randn((10, 512), device="cuda").bfloat16()
+    topk = torch.zeros((0, 4), dtype=torch.int32, device="cuda")
+    o, lse = smla.sparse_mla_fwd(q, kv, topk, None)
+    assert o.numel() == 0 and lse.numel() == 0
+
+
 # -------------------------------------------------------------- backward
 def test_bwd_tiny_full(tiny):
     _check_full(tiny)

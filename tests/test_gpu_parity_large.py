@@ -9,7 +9,8 @@ compute one by one:
   the skewed workload), each computed by the oracle from its full
   contributor list;
 * all of d_sink;
-plus bitwise run-to-run determinism of dq, dkv and d_sink.
+plus bitwise run-to-run determinism of dq, dkv and d_sink; and the forward
+(O and lse) on every token against the oracle's forward.
 
 O and lse, the backward's inputs, come from the oracle's forward over all
 tokens (never from the CUDA path).
@@ -64,11 +65,17 @@ def _sample_rows(topk, N, T, rng, n=64):
     return np.array(sorted(rows), dtype=np.int64)
 
 
-@pytest.mark.parametrize("name", ["headline", "headline_h64_chunked", "t8192_zipf"])
-def test_full_size_sampled_parity_and_determinism(name):
-    spec = W.WORKLOADS[name]
+@pytest.fixture(scope="module", params=["headline", "headline_h64_chunked", "t8192_zipf"])
+def big(request):
+    # module scope with parameters: pytest runs every test of one workload
+    # before building the next, so one set of oracle arrays is alive at a time
+    spec = W.WORKLOADS[request.param]
     inp = W.make_inputs(spec)
-    c = Case(inp)
+    return request.param, spec, inp, Case(inp)
+
+
+def test_full_size_sampled_parity_and_determinism(big):
+    name, spec, inp, c = big
     r_chunk = spec.r_chunk or None
     ws = smla.Workspace()
     out1 = smla.sparse_mla_bwd(c.q, c.kv, c.do, c.o, c.lse, c.topk, c.sink, scale=c.scale,
@@ -95,3 +102,14 @@ def test_full_size_sampled_parity_and_determinism(name):
         compare(f"{name} d_sink", to_f64(dsink), c.ref_dsink())
     else:
         assert dsink is None
+
+
+def test_full_size_forward(big):
+    name, spec, inp, c = big
+    o1, lse1 = smla.sparse_mla_fwd(c.q, c.kv, c.topk, c.sink, scale=c.scale)
+    o2, lse2 = smla.sparse_mla_fwd(c.q, c.kv, c.topk, c.sink, scale=c.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(lse1, lse2), "run-to-run results differ"
+    # c.o64 is the oracle's O rounded to bf16, c.lse64 its lse rounded to fp32
+    compare(f"{name} O", to_f64(o1), c.o64, cos_min=0.99999, rel=1e-2)
+    assert np.max(np.abs(to_f64(lse1) - c.lse64)) < 1e-4
