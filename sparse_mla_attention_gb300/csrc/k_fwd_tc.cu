@@ -13,7 +13,7 @@
 //  * S stage: S = q x kv^T with M = 128 (the heads; lanes >= H unused), N = 256
 //    ranks per rank tile, K = 512 in eight 64-column chunks. The chunk loop is
 //    outermost, so each 64-column q chunk is loaded once per token (TMA, a ring
-//    of two q buffers) and serves every rank tile; kv rows are gathered by the
+//    of three q buffers) and serves every rank tile; kv rows are gathered by the
 //    copy teams. S of rank tile j lives in TMEM columns [256j, 256j + 256).
 //  * Softmax: each epilogue thread owns one head (one TMEM lane): pass 1 takes
 //    the max over the valid ranks and the sink; pass 2 forms e = exp(s - m),
@@ -26,9 +26,11 @@
 //    through a staging tile by TMA.
 // Shared memory: a ring of five 32 KB kv slots (an S-stage use holds 256 rank
 // rows x 64 columns, an O-stage use 128 rank rows x 128 columns as two
-// 64-column blocks), two 16 KB q buffers and four 4 KB staging tiles. Uses are
-// numbered across the CTA's tokens; use g sits in slot g % 5. Copy team k (four
-// warps) fills the uses g = k, k + 4, ...
+// 64-column blocks), three 16 KB q buffers and four 4 KB staging tiles. Uses
+// are numbered across the CTA's tokens; use g sits in slot g % 5. Copy team k
+// (four warps) fills the uses g = k, k + 2, ...: two teams, because more
+// copies in flight per SM made every copy slower (measured with 1 to 5 teams).
+// The next token's q is prefetched into L2 while the current one runs.
 // Every mbarrier wait is bounded; a timeout sets SMLA_ERR_TIMEOUT, stops the
 // CTA's loops, waits (bounded) for its own copies and MMAs and frees TMEM.
 #include "smla_internal.cuh"
@@ -44,9 +46,10 @@ constexpr uint64_t kFtWaitNs = 2000000000ull;
 constexpr float kFtLog2e = 1.4426950408889634f;
 constexpr int kFtSlots = 5;
 constexpr int kFtSlotBytes = 32768;
-constexpr int kFtTeams = 4;
+constexpr int kFtTeams = 2;
 constexpr int kFtTeamWarps = 4;
-constexpr int kFtThreads = (6 + kFtTeams * kFtTeamWarps) * 32;   // TMA, MMA, 4 epilogue, 16 copy
+constexpr int kFtThreads = (6 + kFtTeams * kFtTeamWarps) * 32;   // TMA, MMA, 4 epilogue, 8 copy
+constexpr int kFtQBufs = 3;
 constexpr int kFtQBytes = 128 * 128;                               // up to 128 rows x 64 columns
 constexpr int kFtStageBytes = 32 * 128;
 constexpr int kFtMaxRanks = 512;
@@ -63,7 +66,7 @@ struct FtParams {
 
 struct FtShared {
     uint64_t full[kFtSlots], empty[kFtSlots];
-    uint64_t q_full[2], q_empty[2];
+    uint64_t q_full[kFtQBufs], q_empty[kFtQBufs];
     uint64_t s_full, p_ready, o_full[2], o_empty[2], drain;
     uint32_t tbase;
     volatile int abort_flag;
@@ -71,7 +74,7 @@ struct FtShared {
 };
 
 constexpr int kFtRing = kFtSlots * kFtSlotBytes;
-constexpr int kFtSmem = int(sizeof(FtShared)) + 1024 + kFtRing + 2 * kFtQBytes + 4 * kFtStageBytes;
+constexpr int kFtSmem = int(sizeof(FtShared)) + 1024 + kFtRing + kFtQBufs * kFtQBytes + 4 * kFtStageBytes;
 static_assert(kFtSmem <= 232448, "shared memory of one CTA is at most 227 KB");
 constexpr uint32_t kFtIdescS = idesc_bf16(128, 256, false, false);
 constexpr uint32_t kFtIdescO = idesc_bf16(128, 128, false, true);
@@ -97,12 +100,18 @@ __device__ __forceinline__ bool ft_wait_warp(uint64_t* bar, uint32_t parity,
     return __all_sync(0xffffffffu, ok) != 0;
 }
 
-// Row index of rank r of token t (0 for a masked, invalid or out-of-range rank).
-__device__ __forceinline__ int ft_row(const FtParams& p, int t, int r) {
-    if (r >= p.K) return 0;
-    const int j = __ldg(p.topk + int64_t(t) * p.K + r);
-    if (j < -1 || j >= p.N) { flag_status(p.status, SMLA_ERR_INDEX); return 0; }
-    return j < 0 ? 0 : j;
+// topk[t, r] as stored (-1 past the last rank). Nothing branches on the value
+// here: the copy warps load a use's indices one use ahead and look at them
+// only when that use comes up.
+__device__ __forceinline__ int ft_raw(const FtParams& p, int t, int r) {
+    return r < p.K ? __ldg(p.topk + int64_t(t) * p.K + r) : -1;
+}
+
+// Row to copy for a raw index (row 0 for a masked or invalid one); `bad`
+// collects indices outside [-1, N).
+__device__ __forceinline__ int ft_row_of(int j, int N, bool& bad) {
+    bad |= (j < -1) | (j >= N);
+    return (j >= 0 && j < N) ? j : 0;
 }
 
 }  // namespace
@@ -114,7 +123,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     FtShared& sh = *reinterpret_cast<FtShared*>(smem_raw);
     uint8_t* ring = ft_align1024(smem_raw + sizeof(FtShared));
     uint8_t* qbuf = ring + kFtRing;
-    uint8_t* stage_base = qbuf + 2 * kFtQBytes;
+    uint8_t* stage_base = qbuf + kFtQBufs * kFtQBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nt2 = (p.K + 255) / 256;              // 256-rank tiles of the S stage (1..2)
     const int nt = (p.K + 127) / 128;               // 128-rank tiles of the O stage (1..4)
@@ -127,9 +136,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             mbar_init(&sh.full[s], 32 * kFtTeamWarps);
             mbar_init(&sh.empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kFtQBufs; ++b) {
             mbar_init(&sh.q_full[b], 1);
             mbar_init(&sh.q_empty[b], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
             mbar_init(&sh.o_full[b], 1);
             mbar_init(&sh.o_empty[b], 4);
         }
@@ -152,22 +163,24 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             bool ok = true;
             for (int it = 0; it < ntok && ok; ++it) {
                 const int t = int(blockIdx.x) + it * int(gridDim.x);
+                if (it + 1 < ntok)      // the next token's q into L2 while this one runs
+                    for (int c = 0; c < 8; ++c) tma_prefetch_2d(&map_q, c * 64, (t + int(gridDim.x)) * H);
                 for (int c = 0; c < 8; ++c, ++qi) {
-                    const int b = qi & 1;
-                    ok = ft_wait(&sh.q_empty[b], ((qi >> 1) & 1) ^ 1u, &sh.abort_flag, p.status);
+                    const int b = qi % kFtQBufs;
+                    ok = ft_wait(&sh.q_empty[b], (uint32_t(qi / kFtQBufs) & 1u) ^ 1u, &sh.abort_flag, p.status);
                     if (!ok) break;
                     mbar_arrive_expect_tx(&sh.q_full[b], uint32_t(H) * 128u);
                     tma_load_2d(qbuf + b * kFtQBytes, &map_q, c * 64, t * H, &sh.q_full[b]);
                 }
             }
             if (sh.abort_flag)   // the loads already issued land before the CTA exits
-                for (int k = 1; k <= 2 && qi - k >= 0; ++k)
-                    mbar_wait(&sh.q_full[(qi - k) & 1], ((qi - k) >> 1) & 1, kFtWaitNs / 8);
+                for (int k = 1; k <= kFtQBufs && qi - k >= 0; ++k)
+                    mbar_wait(&sh.q_full[(qi - k) % kFtQBufs], uint32_t((qi - k) / kFtQBufs) & 1u, kFtWaitNs / 8);
         }
         __syncwarp();
     } else if (warp >= 6) {
         // ------------------------------------------ kv gather (copy teams, cp.async)
-        // Team k fills the uses g = k, k + 4, ... An S-stage use (chunk c, rank
+        // Team k fills the uses g = k, k + 2, ... An S-stage use (chunk c, rank
         // tile j) is 256 rank rows x 64 columns: warp wt copies rows
         // 64wt .. 64wt + 63, four rows per round. An O-stage use (chunk c,
         // rank tile j) is 128 rank rows x 128 columns: warp wt copies rows
@@ -178,26 +191,28 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         const int piece = lane & 7;
         const char* kvb = reinterpret_cast<const char*>(p.kv);
         const int total = ntok * uses;
-        // lane's row indices of use g (two for an S-stage use, one for an O-stage use)
+        // lane's raw indices of use g (two for an S-stage use, one for an O-stage use)
         auto load_use = [&](int g, int& r0, int& r1) {
-            r0 = 0; r1 = 0;
+            r0 = -1; r1 = -1;
             if (g >= total) return;
             const int it = g / uses, u = g - it * uses;
             const int t = int(blockIdx.x) + it * int(gridDim.x);
             if (u < 8 * nt2) {
                 const int j = u % nt2;
-                r0 = ft_row(p, t, 256 * j + 64 * wt + lane);
-                r1 = ft_row(p, t, 256 * j + 64 * wt + 32 + lane);
+                r0 = ft_raw(p, t, 256 * j + 64 * wt + lane);
+                r1 = ft_raw(p, t, 256 * j + 64 * wt + 32 + lane);
             } else {
                 const int j = (u - 8 * nt2) % nt;
-                r0 = ft_row(p, t, 128 * j + 32 * wt + lane);
+                r0 = ft_raw(p, t, 128 * j + 32 * wt + lane);
             }
         };
-        int c0, c1;
-        load_use(team, c0, c1);
+        bool bad = false;
+        int raw0, raw1;
+        load_use(team, raw0, raw1);
         for (int g = team; g < total; g += kFtTeams) {
             int n0, n1;
             load_use(g + kFtTeams, n0, n1);
+            const int c0 = ft_row_of(raw0, p.N, bad), c1 = ft_row_of(raw1, p.N, bad);
             const int slot = g % kFtSlots;
             const uint32_t ph = uint32_t(g / kFtSlots) & 1u;
             bool ok = true;
@@ -230,9 +245,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             cp_async_wait<0>();
             fence_proxy_async_smem();
             mbar_arrive(&sh.full[slot]);
-            c0 = n0; c1 = n1;
+            raw0 = n0; raw1 = n1;
         }
         cp_async_wait<0>();
+        if (bad) flag_status(p.status, SMLA_ERR_INDEX);
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -247,8 +263,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                         ++o_drained[b];
                     }
                 for (int c = 0; c < 8 && ok; ++c, ++qi) {
-                    const int b = qi & 1;
-                    ok = ft_wait(&sh.q_full[b], (qi >> 1) & 1, &sh.abort_flag, p.status);
+                    const int b = qi % kFtQBufs;
+                    ok = ft_wait(&sh.q_full[b], uint32_t(qi / kFtQBufs) & 1u, &sh.abort_flag, p.status);
                     if (!ok) break;
                     const uint32_t qa = smem_u32(qbuf + b * kFtQBytes);
                     for (int j = 0; j < nt2 && ok; ++j, ++g) {
