@@ -633,11 +633,13 @@ struct DqShared {
 };
 
 constexpr int kDqSlots = 4;
-// Copy warps: one team of 4 warps per ring slot. Team k fills slot k with the
-// chunks k, k + 4, ... (16 rows per warp), waits for its own copies only and
-// signals the slot, so four chunks are in flight, one per team.
+// Copy warps: four teams of 4 warps. Chunk n of the CTA's sequence sits in slot
+// n % 4; team k fills the chunks n = k, k + 4, ... (16 rows per warp), waits
+// for its own copies only and signals the slot (two teams measured slower).
+constexpr int kDqTeams = 4;
 constexpr int kDqTeamWarps = 4;
-constexpr int kDqCopyWarps = kDqSlots * kDqTeamWarps;
+constexpr int kDqCopyWarps = kDqTeams * kDqTeamWarps;
+static_assert(kDqTeams <= kDqSlots, "parity waits need slots >= teams");
 constexpr int kDqThreads = (6 + kDqCopyWarps) * 32;         // TMA, MMA, 4 epilogue, copy warps
 constexpr int kDqABytes = 2 * 64 * 128;        // two 64-head blocks x 64 ranks
 constexpr int kDqBBytes = 4 * 64 * 128;        // four 64-column blocks x 64 ranks
@@ -657,7 +659,7 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
     const int nkc = p.Rp / 64;
 
     if (threadIdx.x == 0) {
-        // full: the TMA thread's arrive (with the dS bytes) + the 128 threads of the slot's team
+        // full: the TMA thread's arrive (with the dS bytes) + the 128 threads of the chunk's team
         for (int s = 0; s < kDqSlots; ++s) {
             mbar_init(&sh.full[s], 1 + 32 * kDqTeamWarps);  // TMA thread + the slot's team
             mbar_init(&sh.empty[s], 1);
@@ -705,8 +707,8 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
         __syncwarp();
     } else if (warp >= 6) {
         // ------------------------------------------------ kv gather (cp.async)
-        // Team k (warps 4k .. 4k + 3 of the copy warps) fills ring slot k with the
-        // chunks n = k, k + 4, ... of this CTA's chunk sequence; warp w of the team
+        // Team k (warps 4k .. 4k + 3 of the copy warps) fills the chunks
+        // n = k, k + 4, ... of this CTA's chunk sequence (chunk n in slot n % 4); warp w of the team
         // copies rows 16w .. 16w + 15, one row per round: lane l copies the 16-byte
         // piece (l & 7) of 64-column block (l >> 3) of the row's half of D. Lane
         // i < 16 holds the index of row 16w + i, loaded one chunk of the team ahead.
@@ -728,15 +730,16 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
             return j;
         };
         int idx = load_idx(team);
-        uint32_t phase = 0;
-        uint8_t* sbase = slots + team * kDqSlotBytes + kDqABytes;
-        for (int n = team; n < nchunks; n += kDqSlots) {
+        for (int n = team; n < nchunks; n += kDqTeams) {
             const int item = blockIdx.x + (n / nkc) * int(gridDim.x);
+            const int slot = n % kDqSlots;
+            const uint32_t phase = uint32_t(n / kDqSlots) & 1u;
+            uint8_t* sbase = slots + slot * kDqSlotBytes + kDqABytes;
             bool ok = true;
-            if (lane == 0) ok = wait_or_abort(&sh.empty[team], phase ^ 1u, &sh.abort_flag, p.status);
+            if (lane == 0) ok = wait_or_abort(&sh.empty[slot], phase ^ 1u, &sh.abort_flag, p.status);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
-            const int nxt = load_idx(n + kDqSlots);
+            const int nxt = load_idx(n + kDqTeams);
             const char* src0 =
                 reinterpret_cast<const char*>(p.kv) + ((item & 1) * 256 + db * 64) * 2 + piece * 16;
             uint8_t* bt = sbase + db * 8192;
@@ -749,8 +752,7 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
             cp_async_commit();
             cp_async_wait<0>();
             fence_proxy_async_smem();
-            mbar_arrive(&sh.full[team]);
-            phase ^= 1u;
+            mbar_arrive(&sh.full[slot]);
             idx = nxt;
         }
         cp_async_wait<0>();
