@@ -375,11 +375,13 @@ def run_ours(args):
         f_flops = 2 * 2 * 512 * H * W.valid_ranks(inp["topk"])   # S and O GEMMs
         f_tf = f_flops / (ms_f * 1e-3) / 1e12
         tc = H % 32 == 0 and 1 <= K <= 512
+        f_traffic, f_note = _traffic("fwd_tc", T) if tc else (None, None)
         fwd = {"ms_per_call": ms_f, "tflops_valid": f_tf, "calls": args.steps,
                "kernel": "fwd_tc_kernel" if tc else "fwd_kernel",
                "roofline": {"bound": "tensor", "achieved": f_tf, "peak": peaks["bf16_tflops"],
                             "unit": "TFLOP/s", "frac": f_tf / peaks["bf16_tflops"],
-                            "peak_source": peaks["source"] + " bf16 burst"},
+                            "peak_source": peaks["source"] + " bf16 burst",
+                            "traffic": f_traffic, "traffic_note": f_note},
                "flops_valid_per_call": f_flops}
 
     cpu = None
@@ -420,12 +422,15 @@ OVERLAPPED_PHASES = ("csr",)
 # DRAM traffic per launch of the dominant kernels, from one ncu capture (see
 # profiles/), valid only while the kernel source is the one captured.
 _NCU_TRAFFIC = {
-    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "56bdc8853f47ed95"),
-                 "bytes_per_token": (141.410048e6 + 274.877696e6) / 512,
+    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "e768b977278da339"),
+                 "bytes_per_token": (141.388032e6 + 274.550272e6) / 512,
                  "note": "ncu capture of the first 512 tokens, scaled by tokens"},
-    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "56bdc8853f47ed95"),
-                "bytes_per_token": (69.759232e6 + 16.248320e6) / 512,
+    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "e768b977278da339"),
+                "bytes_per_token": (69.766400e6 + 16.238080e6) / 512,
                 "note": "ncu capture of the first 512 tokens, scaled by tokens"},
+    "fwd_tc": {"sources": ("sparse_mla_attention_gb300/csrc/k_fwd_tc.cu", "25328dc02c907a0a"),
+               "bytes_per_token": (72.387072e6 + 17.229824e6) / 512,
+               "note": "ncu capture of the first 512 tokens, scaled by tokens"},
 }
 
 
