@@ -633,10 +633,12 @@ struct DqShared {
 };
 
 constexpr int kDqSlots = 4;
-// Copy warps: four teams of 4 warps. Chunk n of the CTA's sequence sits in slot
-// n % 4; team k fills the chunks n = k, k + 4, ... (16 rows per warp), waits
-// for its own copies only and signals the slot (two teams measured slower).
-constexpr int kDqTeams = 4;
+// Copy warps: two teams of 4 warps. Chunk n of the CTA's sequence sits in slot
+// n % 4; team k fills the chunks n = k, k + 2, ... (16 rows per warp), waits
+// for its own copies only and signals the slot. With four 128-byte rows per
+// copy instruction, two teams measured faster than four (0.42 vs 0.47 ms at
+// T=4096, H=128, topk=512): each copy's latency grows with the copies in flight.
+constexpr int kDqTeams = 2;
 constexpr int kDqTeamWarps = 4;
 constexpr int kDqCopyWarps = kDqTeams * kDqTeamWarps;
 static_assert(kDqTeams <= kDqSlots, "parity waits need slots >= teams");
@@ -708,7 +710,7 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
     } else if (warp >= 6) {
         // ------------------------------------------------ kv gather (cp.async)
         // Team k (warps 4k .. 4k + 3 of the copy warps) fills the chunks
-        // n = k, k + 4, ... of this CTA's chunk sequence (chunk n in slot n % 4); warp w of the team
+        // n = k, k + 2, ... of this CTA's chunk sequence (chunk n in slot n % 4); warp w of the team
         // copies rows 16w .. 16w + 15: per round one 64-column block of four rows, lane l
         // copying the 16-byte piece (l & 7) of row 16w + 4q + (l >> 3) (four rows of 128 bytes
         // per instruction measured faster than one row of 512 bytes). Lane i < 16 holds the
