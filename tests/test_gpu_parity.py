@@ -212,6 +212,10 @@ def test_bwd_t1024_chunked_matches_unchunked(t1024):
     (32, 48, 90, 70, True, 16),     # ragged tiles, chunks
     (64, 200, 260, 130, False, 40), # several rank tiles, no sink, uneven chunk
     (128, 72, 150, 37, True, 0),
+    (48, 100, 150, 40, True, 0),    # the head counts between: odd 16-head chunks,
+    (80, 64, 90, 33, False, 32),    # 64-head stash padding (48), 128-head padding
+    (96, 256, 300, 160, True, 128), # (80, 96, 112), more tokens than SMs (160)
+    (112, 130, 200, 21, True, 0),
 ])
 def test_bwd_custom_shapes(H, K, N, T, sink, chunk):
     c = Case(custom_inputs(H * 7 + K, T=T, H=H, K=K, N=N, sink=sink,
