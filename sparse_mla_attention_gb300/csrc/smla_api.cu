@@ -164,7 +164,11 @@ SideStream* side_stream() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) { cudaGetLastError(); return nullptr; }
     SideStream& ss = per_dev[dev];
     if (!ss.stream) {
-        if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        // greatest priority: the CSR blocks, overlapped with delta, then leave the
+        // SMs to the attention kernels sooner (measured 2.12 -> 2.10 ms per call)
+        int lo = 0, hi = 0;
+        cudaDeviceGetStreamPriorityRange(&lo, &hi);
+        if (cudaStreamCreateWithPriority(&ss.stream, cudaStreamNonBlocking, hi) != cudaSuccess ||
             cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
             cudaGetLastError();
