@@ -101,8 +101,11 @@ int smla_workspace_size(int op, const smla_dims* dims, size_t* bytes);
  * A row with no valid rank gets o = 0 and lse = sink[h] (or -inf without a sink).
  *   q [T,H,D] bf16, kv [num_kv,D] bf16, topk [T,topk] int32, sink [H] fp32 or NULL
  *   -> o [T,H,D] bf16 (round to nearest even), lse [T,H] fp32.
- * This forward exists to produce the backward's inputs; it is a plain CUDA-core
- * kernel, not tuned.
+ * Kernels: for H a multiple of 32 and topk <= 512, a tensor-core kernel
+ * (S and O on tcgen05). It rounds exp(s_r - m) (m = the row max, sink
+ * included) to bf16 as the operand of the O product and divides the fp32
+ * result by the fp32 row sum before rounding o to bf16. Other shapes use a
+ * CUDA-core kernel with fp32 weights.
  */
 int smla_fwd(const uint16_t* q, const uint16_t* kv, const int32_t* topk,
              const float* sink, uint16_t* o, float* lse,
