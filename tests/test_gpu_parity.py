@@ -136,6 +136,22 @@ def test_forward_shapes(H, K, N, T, sink):
     compare("o", o_g, o64, cos_min=0.99999, rel=1e-2)
 
 
+@pytest.mark.parametrize("H", [16, 32, 128])
+def test_forward_topk1_no_sink_is_exact(H):
+    # One valid rank and no sink: the softmax weight is exactly 1, so O is the
+    # selected kv row bit for bit and lse is that rank's score (both kernels:
+    # H = 16 runs on CUDA cores, H = 32 and 128 on the tensor cores).
+    T, N = 200, 300
+    c = custom_inputs(H, T=T, H=H, K=1, N=N, sink=False, mask_p=0.0)
+    case = Case(c)
+    o, lse = smla.sparse_mla_fwd(case.q, case.kv, case.topk, None, scale=case.scale)
+    idx = torch.from_numpy(c["topk"][:, 0].astype(np.int64)).cuda()
+    want = case.kv[idx].unsqueeze(1).expand(T, H, 512)
+    assert torch.equal(o, want)
+    s64 = np.einsum("thd,td->th", case.q64, case.kv64[c["topk"][:, 0]]) * case.scale
+    assert np.max(np.abs(to_f64(lse) - s64)) < 1e-4
+
+
 def test_forward_after_backward_h32():
     # The tensor-core forward runs M = 128 MMAs whatever H is; the TMEM lanes of
     # heads >= H then hold scores of stale shared memory (the previous kernel's
