@@ -113,6 +113,23 @@ def _dist():
     return world, rank, local
 
 
+def _max_over_ranks(x: float, world: int, device) -> float:
+    """The largest `x` over all ranks of the process group (x itself on one rank).
+    Replicas are timed on their own; the job takes as long as the slowest one."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _whole_job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
+    """Throughput of the whole job: every rank's work over the (max-over-ranks) time."""
+    return flops_per_rank * world / (ms * 1e-3) / 1e12
+
+
 def cpu_oracle_sample(spec, inp, seconds: float = 12.0):
     """Times the fp64 oracle backward on a token slice sized to about `seconds`."""
     import numpy as np
@@ -252,15 +269,11 @@ def run_ours(args):
     phases = _lib.profile_read()
     _lib.profiling(False)
     clk = clocks.stop()
-    ms = elapsed_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = _max_over_ranks(elapsed_ms / args.steps, world, dev)
 
     flops = W.flops_valid(inp["topk"], H)
     flops_nom = W.flops_nominal(T, H, K)
-    value = flops * world / (ms * 1e-3) / 1e12
+    value = _whole_job_tflops(flops, world, ms)
     launches = int(sum(p["launches"] for p in phases.values()))
 
     # ---- end to end: host (pinned) inputs -> device -> backward -> host results
@@ -306,12 +319,8 @@ def run_ours(args):
             b_.record(stream)
         torch.cuda.synchronize(dev)
         per_call = sorted(a_.elapsed_time(b_) for a_, b_ in evs)
-        ms_e2e = per_call[len(per_call) // 2]
-        if world > 1:
-            t = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": flops * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOPS",
+        ms_e2e = _max_over_ranks(per_call[len(per_call) // 2], world, dev)
+        e2e = {"value": _whole_job_tflops(flops, world, ms_e2e), "unit": "TFLOPS",
                "ms_per_step": ms_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "calls": n_e2e, "ms_per_step_median_of": "calls",
                "ms_per_step_mean": sum(per_call) / len(per_call),
@@ -371,9 +380,9 @@ def run_ours(args):
             fwd_step()
         f1.record(stream)
         torch.cuda.synchronize(dev)
-        ms_f = f0.elapsed_time(f1) / args.steps
+        ms_f = _max_over_ranks(f0.elapsed_time(f1) / args.steps, world, dev)
         f_flops = 2 * 2 * 512 * H * W.valid_ranks(inp["topk"])   # S and O GEMMs
-        f_tf = f_flops / (ms_f * 1e-3) / 1e12
+        f_tf = _whole_job_tflops(f_flops, world, ms_f)
         tc = H % 32 == 0 and 1 <= K <= 512
         f_traffic, f_note = _traffic("fwd_tc", T) if tc else (None, None)
         fwd = {"ms_per_call": ms_f, "tflops_valid": f_tf, "calls": args.steps,
@@ -397,7 +406,7 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (q, dO, O: 1.5 GB)",
                    "flops_valid_per_step": flops, "flops_nominal_per_step": flops_nom,
-                   "tflops_nominal": flops_nom * world / (ms * 1e-3) / 1e12,
+                   "tflops_nominal": _whole_job_tflops(flops_nom, world, ms),
                    "frac_of_bf16_peak": value / world / peaks["bf16_tflops"]},
         "phases_ms_per_step": {k: v["ms"] / args.steps for k, v in phases.items()},
         "phases_overlapped": list(OVERLAPPED_PHASES),
