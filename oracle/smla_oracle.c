@@ -21,7 +21,7 @@
  *   - delta = rowsum(O * dO) from the given O;
  *   - dKV is the scatter of the per-(t, rank) intermediate
  *     sum_h P*dO + dS*q, inverted into a per-kv-row CSR and gathered.
- * Readings where the page is silent (all from the survey's reading table):
+ * Readings where the page is silent:
  *   sink is a logit in the scaled score domain; lse uses the natural log;
  *   no sink means no denominator term and no d_sink; a row with no valid rank
  *   gets O = 0, lse = sink (or -inf) and contributes no gradient; duplicate
