@@ -125,6 +125,7 @@ struct SdiParams {
     const float* delta;
     uint16_t* interm;     // [T, R, 512]
     int T, K, N, r0, R, Rp, Hp;
+    int ds_rows, ds_off;  // stash rank rows per token; this chunk's first row
     int npairs;           // items per token: ceil(R / 256)
     int tiles_last;       // tiles (1 or 2) in a token's last item
     float scale;
@@ -540,7 +541,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&map_ds, hb * 64, t * p.Rp + row0, stage);
+                        tma_store_2d(&map_ds, hb * 64, t * p.ds_rows + p.ds_off + row0, stage);
                         bulk_commit();
                     }
                     __syncwarp();
@@ -891,9 +892,10 @@ cudaError_t launch_sdi_h(const ChunkArgs& a, cudaStream_t s) {
     if (!make_tmap_bf16_2d(&mq, a.q, uint64_t(a.T) * H, kD, kD, H, 64, true) ||
         !make_tmap_bf16_2d(&mdo, a.dO, uint64_t(a.T) * H, kD, kD, H, 64, true) ||
         !make_tmap_bf16_2d(&mim, a.interm, uint64_t(a.T) * a.R, kD, kD, 32, 64, true) ||
-        !make_tmap_bf16_2d(&mds, a.dsT, uint64_t(a.T) * Rp, Hp, Hp, 32, 64, true))
+        !make_tmap_bf16_2d(&mds, a.dsT, uint64_t(a.T) * a.ds_rows, Hp, Hp, 32, 64, true))
         return cudaErrorInvalidValue;
     SdiParams sp{};
+    sp.ds_rows = a.ds_rows; sp.ds_off = a.ds_off;
     sp.kv = a.kv; sp.topk = a.topk; sp.lse = a.lse; sp.delta = a.delta; sp.interm = a.interm;
     sp.T = a.T; sp.K = a.K; sp.N = a.N; sp.r0 = a.r0; sp.R = a.R; sp.Rp = Rp; sp.Hp = Hp;
     sp.npairs = (a.R + 255) / 256;

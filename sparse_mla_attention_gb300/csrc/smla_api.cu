@@ -81,8 +81,12 @@ BwdPlan plan_bwd(const smla_dims& d) {
     p.off_scan_tmp2 = take(scan_tmp_bytes(p.N));
     p.off_partial = take(size_t(p.max_segs) * kD * 4);
     p.off_interm = take(size_t(nnz_max) * kD * 2);
-    p.off_dst = take(size_t(p.T) * round_up_ranks(int(p.R)) * pad_heads(int(p.H)) * 2);
-    p.off_dqacc = take(p.nchunks > 1 ? size_t(p.T * p.H) * kD * 4 : 0);
+    // With rank chunks of a multiple of 128 ranks the dS^T stash covers all ranks
+    // and dq runs once after the last chunk (no fp32 dq accumulator).
+    p.full_stash = p.nchunks > 1 && p.R % 128 == 0;
+    const int64_t ds_rows = p.full_stash ? p.K : round_up_ranks(int(p.R));
+    p.off_dst = take(size_t(p.T) * ds_rows * pad_heads(int(p.H)) * 2);
+    p.off_dqacc = take(p.nchunks > 1 && !p.full_stash ? size_t(p.T * p.H) * kD * 4 : 0);
     p.off_dkvacc = take(p.nchunks > 1 ? size_t(p.N) * kD * 4 : 0);
     p.bytes = off;
     return p;
@@ -213,9 +217,11 @@ int enqueue_bwd(const BwdArgs& A, const smla_dims& d, const BwdPlan& plan, char*
     int32_t* col = reinterpret_cast<int32_t*>(ws + plan.off_col);
     uint16_t* interm = reinterpret_cast<uint16_t*>(ws + plan.off_interm);
     uint16_t* dsT = reinterpret_cast<uint16_t*>(ws + plan.off_dst);
-    float* dq_acc = plan.nchunks > 1 ? reinterpret_cast<float*>(ws + plan.off_dqacc) : nullptr;
+    float* dq_acc = plan.nchunks > 1 && !plan.full_stash
+                        ? reinterpret_cast<float*>(ws + plan.off_dqacc) : nullptr;
     float* dkv_acc = plan.nchunks > 1 ? reinterpret_cast<float*>(ws + plan.off_dkvacc) : nullptr;
-    const int64_t Rp = round_up_ranks(int(plan.R)), Hp = pad_heads(d.H);
+    const int64_t Hp = pad_heads(d.H);
+    const int64_t ds_rows = plan.full_stash ? plan.K : round_up_ranks(int(plan.R));
     const int whole[2] = {0, d.T};
     const int nt = feed ? feed->n : 1;
     const int* tb = feed ? feed->t : whole;
@@ -253,7 +259,8 @@ int enqueue_bwd(const BwdArgs& A, const smla_dims& d, const BwdPlan& plan, char*
             a.T = t1 - t0; a.H = d.H; a.K = d.topk; a.N = d.num_kv; a.r0 = r0; a.R = int(plan.R);
             a.scale = scale;
             a.interm = interm + int64_t(t0) * plan.R * kD;
-            a.dsT = dsT + int64_t(t0) * Rp * Hp;
+            a.dsT = dsT + int64_t(t0) * ds_rows * Hp;
+            a.ds_rows = int(ds_rows); a.ds_off = plan.full_stash ? r0 : 0;
             a.dq_acc = dq_acc ? dq_acc + th * kD : nullptr;
             a.dq_out = A.dq + th * kD;
             a.first_chunk = first; a.last_chunk = last; a.status = status;
@@ -261,9 +268,16 @@ int enqueue_bwd(const BwdArgs& A, const smla_dims& d, const BwdPlan& plan, char*
                 prof::Scope ph(prof::kSdi, s);
                 if ((rc = cuda_rc(launch_attn_sdi(a, s)))) return rc;
             }
-            {
+            if (!plan.full_stash) {
                 prof::Scope ph(prof::kDq, s);
                 if ((rc = cuda_rc(launch_attn_dq(a, s)))) return rc;
+            } else if (last) {
+                // dq over all ranks from the full stash, once
+                ChunkArgs b = a;
+                b.r0 = 0; b.R = int(plan.K); b.ds_off = 0;
+                b.first_chunk = b.last_chunk = true; b.dq_acc = nullptr;
+                prof::Scope ph(prof::kDq, s);
+                if ((rc = cuda_rc(launch_attn_dq(b, s)))) return rc;
             }
             if (last && feed && (rc = cuda_rc(cudaEventRecord(feed->dq_ready[i], s)))) return rc;
         }

@@ -77,6 +77,7 @@ CsrPlan plan_csr(int64_t T, int64_t r_len, int64_t num_kv);
 struct BwdPlan {
     int64_t T, H, K, N, R;   // R = rank chunk
     int nchunks;
+    bool full_stash;         // chunked, R a multiple of 128: one dS^T stash of all ranks
     CsrPlan csr;
     int64_t max_segs;
     size_t off_delta, off_rowptr, off_col, off_csr, off_segptr, off_segrow, off_segcnt,
@@ -119,14 +120,18 @@ cudaError_t launch_fwd_tc(const uint16_t* q, const uint16_t* kv, const int32_t* 
                           int num_kv, float scale, unsigned* status, cudaStream_t s);
 
 // Per-chunk attention backward core: for ranks [r0, r0+R) of each token, builds
-// interm [T, R, D] bf16 (sum_h P*dO + scale*dS*q) and dsT [T, R, H] bf16
-// (scale * dS, transposed), then accumulates dq.
+// interm [T, R, D] bf16 (sum_h P*dO + scale*dS*q) and the scale*dS^T stash
+// (bf16, heads padded to Hp), then accumulates dq. The stash has ds_rows rank
+// rows per token and the chunk's rows start at ds_off: round_up(R, 128) and 0
+// for a stash of the chunk alone, or topk and r0 for one stash of all ranks
+// (then dq runs once over all ranks, after the last chunk).
 struct ChunkArgs {
     const uint16_t* q; const uint16_t* kv; const uint16_t* dO;
     const float* lse; const float* delta; const int32_t* topk;
     int T, H, K, N, r0, R;
     float scale;
     uint16_t* interm; uint16_t* dsT;
+    int ds_rows, ds_off;
     float* dq_acc; uint16_t* dq_out;   // dq_acc NULL when unchunked
     bool first_chunk, last_chunk;
     unsigned* status;
