@@ -431,11 +431,11 @@ OVERLAPPED_PHASES = ("csr",)
 # DRAM traffic per launch of the dominant kernels, from one ncu capture (see
 # profiles/), valid only while the kernel source is the one captured.
 _NCU_TRAFFIC = {
-    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "317626adebf34d7e"),
-                 "bytes_per_token": (141.007360e6 + 274.786816e6) / 512,
+    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "a9366e6493ee301b"),
+                 "bytes_per_token": (141.261568e6 + 274.870272e6) / 512,
                  "note": "ncu capture of the first 512 tokens, scaled by tokens"},
-    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "317626adebf34d7e"),
-                "bytes_per_token": (69.761792e6 + 15.819264e6) / 512,
+    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "a9366e6493ee301b"),
+                "bytes_per_token": (69.764096e6 + 15.354880e6) / 512,
                 "note": "ncu capture of the first 512 tokens, scaled by tokens"},
     "fwd_tc": {"sources": ("sparse_mla_attention_gb300/csrc/k_fwd_tc.cu", "3275cc58b29baa34"),
                "bytes_per_token": (72.340224e6 + 16.913664e6) / 512,
