@@ -1,5 +1,6 @@
-// k_fwd.cu -- sparse MLA forward on CUDA cores (produces O and lse for the
-// backward's inputs; not a tuned kernel).
+// k_fwd.cu -- sparse MLA forward on CUDA cores, for the shapes the tensor-core
+// forward (k_fwd_tc.cu) does not take: H not a multiple of 32, or topk > 512.
+// launch_fwd tries the tensor-core kernel first. Not a tuned kernel.
 //
 // Definition (aiter "Sparse MLA training backward", Contract section and the
 // lse paragraph under its usage example): for token t, head h and the valid
