@@ -68,7 +68,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -111,6 +111,16 @@ def _dist():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def _busy(step, dev, seconds: float) -> None:
+    """Runs `step` untimed for about `seconds` (synchronising every few steps)."""
+    import torch
+    t_end = time.perf_counter() + seconds
+    while time.perf_counter() < t_end:
+        for _ in range(4):
+            step()
+        torch.cuda.synchronize(dev)
 
 
 def _max_over_ranks(x: float, world: int, device) -> float:
@@ -252,6 +262,10 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     clocks = ClockSampler(local)
     clocks.start()
+    # the clock samples (every 100 ms) should see the GPU under this load: the
+    # same step runs untimed for about 0.4 s before and 0.3 s after the K timed
+    # steps (the timed region itself lasts only K steps)
+    _busy(step, dev, 0.4)
     _lib.profiling(True)
     if world > 1:
         dist.barrier()
@@ -268,6 +282,7 @@ def run_ours(args):
     elapsed_ms = e0.elapsed_time(e1)
     phases = _lib.profile_read()
     _lib.profiling(False)
+    _busy(step, dev, 0.3)
     clk = clocks.stop()
     ms = _max_over_ranks(elapsed_ms / args.steps, world, dev)
 
