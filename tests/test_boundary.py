@@ -131,6 +131,20 @@ def test_workspace_size_grows_with_chunks(lib):
     assert lib.smla_workspace_size(7, ctypes.byref(d), ctypes.byref(n)) == _lib.SMLA_ERR_ARG
 
 
+def test_chunks_of_128_ranks_need_no_dq_accumulator(lib):
+    def ws(**kw):
+        d = SmlaDims(**{**BASE, "T": 4096, "H": 128, "topk": 512, "num_kv": 5120, **kw})
+        n = ctypes.c_size_t()
+        assert lib.smla_workspace_size(_lib.SMLA_OP_BWD, ctypes.byref(d), ctypes.byref(n)) == 0
+        return n.value
+    acc = 4096 * 128 * 512 * 4          # the fp32 dq accumulator of per-chunk dq: 1 GiB
+    # r_chunk = 64 keeps a per-chunk dS^T stash and the fp32 dq accumulator; r_chunk = 128
+    # (a multiple of 128) keeps one stash over all ranks and runs dq once, without it
+    assert ws(r_chunk=64) > acc
+    assert ws(r_chunk=128) < ws(r_chunk=64)
+    assert ws(r_chunk=128) - ws(r_chunk=256) < acc
+
+
 def test_csr_build_validation(lib):
     a = _addrs()
     big = ctypes.c_size_t(1 << 40).value
