@@ -212,3 +212,14 @@ def test_bwd_host_validation(lib):
         return
     a = _addrs(); a["lse"] = ctypes.c_void_p(a["lse"].value + 4)
     assert _bwd_host(lib, dims, a) in (_lib.SMLA_ERR_CUDA, _lib.SMLA_ERR_ARCH)
+
+
+def test_missing_library_fails_loudly():
+    # no fallback: loading a library that is not there raises (fresh process, nothing cached)
+    import subprocess
+    import sys
+    code = ("from sparse_mla_attention_gb300 import _lib\n"
+            "_lib.load('/nonexistent/libsmla.so')\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                       cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert r.returncode != 0 and "not found" in r.stderr
