@@ -8,22 +8,27 @@
 //   lse = m + ln(l),   O[t,h,:] = sum_r exp(s_r - m) * kv[idx_r,:] / l
 // (no sink term without a sink). The last form equals sum_r exp(s_r - lse) kv.
 //
-// fwd_tc_kernel: persistent, one CTA per SM, work item = one token (topk <= 512,
-// H a multiple of 32 up to 128).
+// fwd_tc_kernel: persistent, one CTA per SM (TMA warp, MMA warp, 8 epilogue
+// warps, 8 copy warps), work item = one token (topk <= 512, H a multiple of 32
+// up to 128).
 //  * S stage: S = q x kv^T with M = 128 (the heads; lanes >= H unused), N = 256
 //    ranks per rank tile, K = 512 in eight 64-column chunks. The chunk loop is
 //    outermost, so each 64-column q chunk is loaded once per token (TMA, a ring
 //    of three q buffers) and serves every rank tile; kv rows are gathered by the
 //    copy teams. S of rank tile j lives in TMEM columns [256j, 256j + 256).
-//  * Softmax: each epilogue thread owns one head (one TMEM lane): pass 1 takes
-//    the max over the valid ranks and the sink; pass 2 forms e = exp(s - m),
-//    sums it, and writes bf16(e) pairs back over S columns already read
-//    (ranks 2c, 2c + 1 in column c: P' in [0, ranks / 2)).
+//  * Softmax: two epilogue warps per TMEM lane quarter (one thread per head),
+//    each over half of the 32-rank groups: pass 1 takes the max over the valid
+//    ranks (the two halves swap theirs; the sink joins), pass 2 forms
+//    e = exp(s - m), sums it, and writes bf16(e) pairs over S columns already
+//    read: half 0 in ascending group order at column 16gq, half 1 in descending
+//    order at column 16ng + 16gq (ng groups in all). Half 1 hands its sum to
+//    half 0, which writes lse and drains O.
 //  * O stage: O' = P' x kv with A = P' from TMEM, M = 128, N = 128 columns of D
 //    per chunk, K = 128 ranks per use (kv rows gathered again, MN-major). The
-//    chunk accumulators alternate between TMEM columns [256, 384) and
-//    [384, 512); the drain scales a row by 1/l, rounds to bf16 and stores it
-//    through a staging tile by TMA.
+//    two chunk accumulators lie between the two halves' P' (columns
+//    [128, 384) for 512 ranks, [256, 512) for 256) and alternate; the drain
+//    scales a row by 1/l, rounds to bf16 and stores it through a staging tile
+//    by TMA.
 // Shared memory: a ring of five 32 KB kv slots (an S-stage use holds 256 rank
 // rows x 64 columns, an O-stage use 128 rank rows x 128 columns as two
 // 64-column blocks), three 16 KB q buffers and four 4 KB staging tiles. Uses
@@ -48,7 +53,9 @@ constexpr int kFtSlots = 5;
 constexpr int kFtSlotBytes = 32768;
 constexpr int kFtTeams = 2;
 constexpr int kFtTeamWarps = 4;
-constexpr int kFtThreads = (6 + kFtTeams * kFtTeamWarps) * 32;   // TMA, MMA, 4 epilogue, 8 copy
+constexpr int kFtEpiWarps = 8;                                     // two per TMEM lane quarter
+constexpr int kFtCopyWarp0 = 2 + kFtEpiWarps;
+constexpr int kFtThreads = (kFtCopyWarp0 + kFtTeams * kFtTeamWarps) * 32;   // TMA, MMA, 8 epilogue, 8 copy
 constexpr int kFtQBufs = 3;
 constexpr int kFtQBytes = 128 * 128;                               // up to 128 rows x 64 columns
 constexpr int kFtStageBytes = 32 * 128;
@@ -68,9 +75,12 @@ struct FtShared {
     uint64_t full[kFtSlots], empty[kFtSlots];
     uint64_t q_full[kFtQBufs], q_empty[kFtQBufs];
     uint64_t s_full, p_ready, o_full[2], o_empty[2], drain;
+    uint64_t xchg[4], sum_bar[4];          // per lane quarter: the two halves' max / sum hand-over
     uint32_t tbase;
     volatile int abort_flag;
-    uint32_t valid[4][kFtMaxRanks / 32];   // per epilogue warp: valid-rank bits of the token
+    uint32_t valid[kFtEpiWarps][kFtMaxRanks / 64];   // per epilogue warp: its groups' valid-rank bits
+    float red_max[2][128];                 // per half and head: the half's max score
+    float red_sum[128];                    // per head: half 1's sum of exp(s - m)
 };
 
 constexpr int kFtRing = kFtSlots * kFtSlotBytes;
@@ -128,6 +138,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     const int nt2 = (p.K + 255) / 256;              // 256-rank tiles of the S stage (1..2)
     const int nt = (p.K + 127) / 128;               // 128-rank tiles of the O stage (1..4)
     const int uses = 8 * nt2 + 4 * nt;              // kv uses per token
+    const int ng = 8 * nt2;                         // 32-rank groups of S
+    // TMEM after the softmax: P' of half 0 in [0, 8ng), of half 1 in [24ng, 32ng); the
+    // two O accumulators sit between them (ng = 16) or above S (ng = 8)
+    const int acc0 = ng == 16 ? 128 : 256;
     const int ntok = (p.T - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x);
     const int H = p.H;
 
@@ -145,7 +159,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             mbar_init(&sh.o_empty[b], 4);
         }
         mbar_init(&sh.s_full, 1);
-        mbar_init(&sh.p_ready, 4);
+        mbar_init(&sh.p_ready, kFtEpiWarps);
+        for (int q = 0; q < 4; ++q) {
+            mbar_init(&sh.xchg[q], 2);     // lane 0 of each of the quarter's two warps
+            mbar_init(&sh.sum_bar[q], 1);  // lane 0 of the quarter's half-1 warp
+        }
         mbar_init(&sh.drain, 1);
         sh.abort_flag = 0;
         fence_mbar_init();
@@ -178,7 +196,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                     mbar_wait(&sh.q_full[(qi - k) % kFtQBufs], uint32_t((qi - k) / kFtQBufs) & 1u, kFtWaitNs / 8);
         }
         __syncwarp();
-    } else if (warp >= 6) {
+    } else if (warp >= kFtCopyWarp0) {
         // ------------------------------------------ kv gather (copy teams, cp.async)
         // Team k fills the uses g = k, k + 2, ... An S-stage use (chunk c, rank
         // tile j) is 256 rank rows x 64 columns: warp wt copies rows
@@ -187,7 +205,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         // 64-column block at a time. Every copy instruction covers four rows of
         // 128 bytes (measured faster than fewer, longer rows).
         // The row indices of the team's next use are loaded during this one.
-        const int gw = warp - 6;
+        const int gw = warp - kFtCopyWarp0;
         const int team = gw / kFtTeamWarps, wt = gw % kFtTeamWarps;
         const int piece = lane & 7;
         const char* kvb = reinterpret_cast<const char*>(p.kv);
@@ -303,9 +321,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t sb = smem_u32(ring + slot * kFtSlotBytes);
+                        // P' of rank tile j: half 0's groups at 64j, half 1's at 16ng + 64j
+                        const uint32_t pa = tbase + (j < nt2 ? 64 * j : 16 * ng + 64 * j);
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
-                            mma_ts(tbase + 256 + 128 * b, tbase + 64 * j + 8 * k,
+                            mma_ts(tbase + acc0 + 128 * b, pa + 8 * k,
                                    sdesc_sw128(sb + k * 2048, 16384, 1024), kFtIdescO, (j | k) != 0);
                         mma_commit(&sh.empty[slot]);
                     }
@@ -320,16 +340,24 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         __syncwarp();
     } else {
         // ------------------------------------------------------ softmax + O drain
+        // Two warps per TMEM lane quarter: half 0 (warps 2-5) takes the rank groups
+        // [0, ng/2), half 1 (warps 6-9) the groups [ng/2, ng). Each writes P' over
+        // S columns it has already read: half 0 group gq at 16gq (ascending order),
+        // half 1 group gq at 16ng + 16gq (descending order: that column range
+        // belongs to S group ng/2 + gq/2 >= gq, read first). The halves swap their
+        // maxima, half 1 hands its sum to half 0, and half 0 drains O.
+        const int ew = warp - 2;
+        const int half = ew >> 2;
         const int quarter = warp & 3;
         const int h = quarter * 32 + lane;              // this thread's head (TMEM lane)
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-        const int ew = warp - 2;
         uint32_t* vmask = sh.valid[ew];
-        uint8_t* stage = stage_base + ew * kFtStageBytes;
+        uint8_t* stage = stage_base + (ew & 3) * kFtStageBytes;
         const bool store_rows = quarter * 32 < H;       // H is a multiple of 32
         const float sink_h = (p.sink && h < H) ? __ldg(p.sink + h) : -INFINITY;
         const float c1 = p.scale * kFtLog2e;
-        const int ng = 8 * nt2;                         // 32-rank groups of S
+        const int nh = ng / 2;                          // groups per half (4 or 8)
+        const int gbeg = half * nh;
         // The TMEM loads below are warp-collective: every lane runs every load,
         // and per-lane conditions only select which loaded values count.
         // Lanes of heads >= H (rows of the q tile left stale) count no rank.
@@ -338,12 +366,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         for (int it = 0; it < ntok; ++it) {
             const int t = int(blockIdx.x) + it * int(gridDim.x);
             if (__any_sync(0xffffffffu, sh.abort_flag != 0)) break;
-            // valid-rank bits of the token (each warp its own copy)
+            // valid-rank bits of this warp's groups
 #pragma unroll
-            for (int m = 0; m < kFtMaxRanks / 32; ++m) {
-                const int r = 32 * m + lane;
+            for (int m = 0; m < kFtMaxRanks / 64; ++m) {
+                const int r = 32 * (gbeg + m) + lane;
                 bool v = false;
-                if (r < p.K) {
+                if (m < nh && r < p.K) {
                     const int j = __ldg(p.topk + int64_t(t) * p.K + r);
                     v = j >= 0 && j < p.N;
                 }
@@ -354,31 +382,38 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             if (!ft_wait_warp(&sh.s_full, it & 1, &sh.abort_flag, p.status)) break;
             tc_fence_after();
             const uint32_t trow = tbase + lane_off;
-            // pass 1: max of the valid scores
+            // pass 1: max of the valid scores of this half, then of both halves
             float mx = -INFINITY;
 #pragma unroll 1
-            for (int gq = 0; gq < ng; ++gq) {
+            for (int m = 0; m < nh; ++m) {
                 uint32_t v[32];
-                tmem_ld32(trow + 32 * gq, v);
+                tmem_ld32(trow + 32 * (gbeg + m), v);
                 tmem_wait_ld();
-                const uint32_t bits = vmask[gq] & live;
+                const uint32_t bits = vmask[m] & live;
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
                     if ((bits >> e) & 1u) mx = fmaxf(mx, __uint_as_float(v[e]));
             }
+            sh.red_max[half][h] = mx;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.xchg[quarter]);
+            if (!ft_wait_warp(&sh.xchg[quarter], it & 1, &sh.abort_flag, p.status)) break;
+            mx = fmaxf(mx, sh.red_max[half ^ 1][h]);
             // m = max(sink, scale * max s)
             const float m = fmaxf(sink_h, mx * p.scale);
             const bool any = m != -INFINITY;
             const float mb = any ? m * kFtLog2e : 0.f;
-            float sum = (p.sink && any) ? ex2_approx((sink_h - m) * kFtLog2e) : 0.f;
-            // pass 2: e = exp(s - m) summed, and written as bf16 pairs over
-            // columns already read (group gq -> columns [16gq, 16gq + 16))
+            // pass 2: e = exp(s - m) summed, and written as bf16 pairs over columns
+            // already read
+            float psum = 0.f;
 #pragma unroll 1
-            for (int gq = 0; gq < ng; ++gq) {
+            for (int mm = 0; mm < nh; ++mm) {
+                const int m_i = half == 0 ? mm : nh - 1 - mm;
+                const int gq = gbeg + m_i;
                 uint32_t v[32];
                 tmem_ld32(trow + 32 * gq, v);
                 tmem_wait_ld();
-                const uint32_t bits = any ? (vmask[gq] & live) : 0u;
+                const uint32_t bits = any ? (vmask[m_i] & live) : 0u;
                 uint32_t pp[16];
 #pragma unroll
                 for (int e2 = 0; e2 < 16; ++e2) {
@@ -386,16 +421,28 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                                         ? ex2_approx(fmaf(__uint_as_float(v[2 * e2]), c1, -mb)) : 0.f;
                     const float b = ((bits >> (2 * e2 + 1)) & 1u)
                                         ? ex2_approx(fmaf(__uint_as_float(v[2 * e2 + 1]), c1, -mb)) : 0.f;
-                    sum += a + b;
+                    psum += a + b;
                     pp[e2] = pack_bf16x2(a, b);
                 }
-                tmem_st8(trow + 16 * gq, pp);
-                tmem_st8(trow + 16 * gq + 8, pp + 8);
+                const uint32_t pcol = half == 0 ? 16 * gq : 16 * ng + 16 * gq;
+                tmem_st8(trow + pcol, pp);
+                tmem_st8(trow + pcol + 8, pp + 8);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.p_ready);
+            if (half == 1) {
+                // hand the sum to half 0 (which drains O); red_sum is rewritten only
+                // after half 0 has read it: the next token's S stage waits for the drains
+                sh.red_sum[h] = psum;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.sum_bar[quarter]);
+                continue;
+            }
+            if (!ft_wait_warp(&sh.sum_bar[quarter], it & 1, &sh.abort_flag, p.status)) break;
+            float sum = (p.sink && any) ? ex2_approx((sink_h - m) * kFtLog2e) : 0.f;
+            sum += psum + sh.red_sum[h];
             const float lse = any ? m + logf(sum) : -INFINITY;
             if (h < H) p.lse[int64_t(t) * H + h] = lse;
             const float inv = sum > 0.f ? 1.f / sum : 0.f;
@@ -419,7 +466,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 #pragma unroll 1
                     for (int gq = 0; gq < 2; ++gq) {
                         uint32_t v[32];
-                        tmem_ld32(trow + 256 + 128 * b + 64 * hh + 32 * gq, v);
+                        tmem_ld32(trow + acc0 + 128 * b + 64 * hh + 32 * gq, v);
                         tmem_wait_ld();
                         if (hh == 1 && gq == 1) {       // the accumulator is read: the MMA may reuse it
                             tc_fence_before();
