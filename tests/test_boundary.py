@@ -223,3 +223,18 @@ def test_missing_library_fails_loudly():
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
                        cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
     assert r.returncode != 0 and "not found" in r.stderr
+
+
+def test_python_api_refuses_cpu_tensors():
+    # the product path has no CPU fallback: host tensors are rejected before any call
+    import torch
+    import sparse_mla_attention_gb300 as smla
+    T, H, K, N = 4, 16, 8, 10
+    q = torch.zeros((T, H, 512), dtype=torch.bfloat16)
+    kv = torch.zeros((N, 512), dtype=torch.bfloat16)
+    topk = torch.zeros((T, K), dtype=torch.int32)
+    lse = torch.zeros((T, H), dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        smla.sparse_mla_fwd(q, kv, topk)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        smla.sparse_mla_bwd(q, kv, q, q, lse, topk)
