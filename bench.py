@@ -140,6 +140,41 @@ def _whole_job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
     return flops_per_rank * world / (ms * 1e-3) / 1e12
 
 
+def _percentiles(ms_list) -> dict:
+    """Median, p10, p90, mean, min and max of a list of per-call times (ms)."""
+    s = sorted(float(x) for x in ms_list)
+    if not s:
+        return {}
+
+    def pct(p):
+        # linear interpolation between order statistics
+        k = (len(s) - 1) * p
+        lo = int(k)
+        hi = min(lo + 1, len(s) - 1)
+        return s[lo] + (s[hi] - s[lo]) * (k - lo)
+    return {"median": pct(0.5), "p10": pct(0.1), "p90": pct(0.9), "mean": sum(s) / len(s),
+            "min": s[0], "max": s[-1], "n": len(s)}
+
+
+def _cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_oracle_sample(spec, inp, seconds: float = 12.0):
     """Times the fp64 oracle backward on a token slice sized to about `seconds`."""
     import numpy as np
@@ -167,10 +202,12 @@ def cpu_oracle_sample(spec, inp, seconds: float = 12.0):
     n = int(max(4, min(spec.T - t0, 4 * seconds / max(dt, 1e-3))))
     dt, fl = run(n)
     return {"value": fl / dt / 1e12, "unit": "TFLOPS", "cores": oracle.threads(),
-            "kind": "oracle",
+            "cpu_model": _cpu_model(), "kind": "oracle",
             "sample": f"full fp64 backward (dq, dkv scatter, d_sink) of tokens "
-                      f"{t0}..{t0 + n - 1} of the {spec.name} workload ({dt:.1f} s)",
-            "ms_per_token": dt * 1e3 / n}
+                      f"{t0}..{t0 + n - 1} of the {spec.name} workload ({dt:.1f} s); TFLOPS over "
+                      f"that slice's valid triples, extrapolated to the whole workload at the "
+                      f"same rate",
+            "extrapolated": True, "ms_per_token": dt * 1e3 / n}
 
 
 def run_reference(args):
@@ -199,8 +236,11 @@ def run_reference(args):
         "data": "synthetic",
         "config": {"workload": spec.name, "shape": spec.describe(),
                    "note": "each step times the fp64 oracle on a bounded token slice; "
-                           "ms_per_step extrapolates to the whole workload"},
-        "cpu_baseline": {"kind": res["kind"], "cores": res["cores"], "sample": res["sample"],
+                           "ms_per_step is extrapolated to the whole workload from that "
+                           "slice's rate (not measured over the whole workload)",
+                   "ms_per_step_extrapolated": True},
+        "cpu_baseline": {"kind": res["kind"], "cores": res["cores"], "cpu_model": res["cpu_model"],
+                         "sample": res["sample"], "extrapolated": True,
                          "value": value, "unit": "TFLOPS"},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -266,25 +306,33 @@ def run_ours(args):
     # same step runs untimed for about 0.4 s before and 0.3 s after the K timed
     # steps (the timed region itself lasts only K steps)
     _busy(step, dev, 0.4)
-    _lib.profiling(True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    # K + 1 events on the launching stream: the region e[0] -> e[K] is the timed
+    # total (its mean is ms_per_step); e[i] -> e[i+1] is call i (median, p10, p90)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
+    for i in range(args.steps):
+        step()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = evs[0].elapsed_time(evs[-1])
+    per_call = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    # the phase split comes from a second, untimed pass of the same K steps with
+    # the library's phase events on (no profiler event inside the timed region)
+    _lib.profiling(True)
     for _ in range(args.steps):
         step()
-    e1.record(stream)
     torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    elapsed_ms = e0.elapsed_time(e1)
     phases = _lib.profile_read()
     _lib.profiling(False)
     _busy(step, dev, 0.3)
     clk = clocks.stop()
     ms = _max_over_ranks(elapsed_ms / args.steps, world, dev)
+    call_stats = _percentiles(per_call)
 
     flops = W.flops_valid(inp["topk"], H)
     flops_nom = W.flops_nominal(T, H, K)
@@ -340,6 +388,7 @@ def run_ours(args):
                "calls": n_e2e, "ms_per_step_median_of": "calls",
                "ms_per_step_mean": sum(per_call) / len(per_call),
                "ms_per_step_min": per_call[0], "ms_per_step_max": per_call[-1],
+               "per_call_ms": _percentiles(per_call),
                "api": "smla_bwd_host (host buffers, copies pipelined by token chunks)"}
 
     # ---- roofline of the dominant kernel (live CUDA-event phase times)
@@ -388,19 +437,19 @@ def run_ours(args):
         if smla.device_status(ws_f.buf) != 0:
             raise RuntimeError("device status set by the forward")
         torch.cuda.synchronize(dev)
-        f0 = torch.cuda.Event(enable_timing=True)
-        f1 = torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        for _ in range(args.steps):
+        fev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        fev[0].record(stream)
+        for i in range(args.steps):
             fwd_step()
-        f1.record(stream)
+            fev[i + 1].record(stream)
         torch.cuda.synchronize(dev)
-        ms_f = _max_over_ranks(f0.elapsed_time(f1) / args.steps, world, dev)
+        ms_f = _max_over_ranks(fev[0].elapsed_time(fev[-1]) / args.steps, world, dev)
+        f_calls = _percentiles(fev[i].elapsed_time(fev[i + 1]) for i in range(args.steps))
         f_flops = 2 * 2 * 512 * H * W.valid_ranks(inp["topk"])   # S and O GEMMs
         f_tf = _whole_job_tflops(f_flops, world, ms_f)
         tc = H % 32 == 0 and 1 <= K <= 512
         f_traffic, f_note = _traffic("fwd_tc", T) if tc else (None, None)
-        fwd = {"ms_per_call": ms_f, "tflops_valid": f_tf, "calls": args.steps,
+        fwd = {"ms_per_call": ms_f, "tflops_valid": f_tf, "calls": args.steps, "per_call_ms": f_calls,
                "kernel": "fwd_tc_kernel" if tc else "fwd_kernel",
                "roofline": {"bound": "tensor", "achieved": f_tf, "peak": peaks["bf16_tflops"],
                             "unit": "TFLOP/s", "frac": f_tf / peaks["bf16_tflops"],
@@ -423,7 +472,9 @@ def run_ours(args):
                    "flops_valid_per_step": flops, "flops_nominal_per_step": flops_nom,
                    "tflops_nominal": _whole_job_tflops(flops_nom, world, ms),
                    "frac_of_bf16_peak": value / world / peaks["bf16_tflops"]},
+        "per_call_ms": call_stats,
         "phases_ms_per_step": {k: v["ms"] / args.steps for k, v in phases.items()},
+        "phases_note": "CUDA-event phase times from a separate untimed pass of the same steps",
         "phases_overlapped": list(OVERLAPPED_PHASES),
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -440,8 +491,10 @@ def run_ours(args):
     return 0
 
 
-# Phases the library runs on its side stream, overlapped with the others.
-OVERLAPPED_PHASES = ("csr",)
+# Phases that run concurrently with others (the CSR build and dq on the
+# library's side stream, the dKV gather beside dq): their event spans are not
+# their own run times.
+OVERLAPPED_PHASES = ("csr", "attn_dq", "gather")
 
 # DRAM traffic per launch of the dominant kernels, from one ncu capture (see
 # profiles/), valid only while the kernel source is the one captured.
@@ -497,8 +550,8 @@ def _algorithmic(phase: str, spec, topk):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
