@@ -20,7 +20,11 @@
  *     caller (HOST buffers for smla_bwd_host): q, dO, o, dq are [T, H, D];
  *     kv, dkv are [num_kv, D]; lse is [T, H]; topk is [T, topk]; sink, d_sink
  *     are [H]. bf16 tensors are passed as uint16_t bit patterns.
- *   - Every device pointer must be 16-byte aligned.
+ *   - Every device pointer must be 16-byte aligned, and must point to device
+ *     (or managed) memory of the current device: each is checked with
+ *     cudaPointerGetAttributes before anything is enqueued (SMLA_ERR_DEVICE).
+ *     The library cannot see how long a caller's buffer is: each must hold
+ *     the tensor that the shape says.
  *   - The library allocates no device memory during a call. The caller passes
  *     a device workspace of at least smla_workspace_size() bytes. Between calls
  *     the library keeps a per-device cache of the arch check and, per host
@@ -64,7 +68,9 @@ enum smla_status {
     SMLA_ERR_INDEX = 11,        /* device: a topk entry outside [-1, num_kv) was seen */
     SMLA_ERR_TIMEOUT = 12,      /* device: a bounded wait inside a kernel ran out */
     SMLA_ERR_SINK = 13,         /* d_sink given without sink, or sink without d_sink */
-    SMLA_ERR_ARG = 14           /* any other invalid argument (e.g. a non-finite scale) */
+    SMLA_ERR_ARG = 14,          /* any other invalid argument (e.g. a non-finite scale) */
+    SMLA_ERR_DEVICE = 15        /* a pointer that must be device memory is not device (or managed)
+                                   memory of the current device */
 };
 
 /* Problem dimensions. */
@@ -194,12 +200,28 @@ int smla_csr_build(const int32_t* topk, int32_t T, int32_t topk_w, int32_t r0,
  *   - The array exists on every GPU that loads the library, until the process exits.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture. The address belongs to the device's current
+ *     CUDA context: after cudaDeviceReset the first call in the new context
+ *     looks it up again (same rule).
  *   - All calls share the array: calls whose kernels overlap on the GPU race,
  *     so serialize them (one stream, or events between streams).
  */
 int smla_dsink_static(const uint16_t* dO, const uint16_t* o, const float* lse,
                       const float* sink, float* d_sink, int32_t T, int32_t H, void* stream);
+
+/*
+ * Self-test of the kernels' bounded waits (the pages have no counterpart; it
+ * exists so that the failure path can be exercised without faulting a GPU).
+ * Launches one CTA that waits on an mbarrier nothing arrives on, through the
+ * same wait-and-unwind code as the tensor-core kernels, with a limit of
+ * `limit_us` microseconds (1 .. 1000000): the wait runs out, the CTA sets
+ * SMLA_ERR_TIMEOUT in the workspace's status word, stops its other warps,
+ * frees its tensor memory and exits. Read the result with
+ * smla_get_device_status(); the device stays usable afterwards.
+ *   workspace: device memory of at least 256 bytes (its status word is reset).
+ */
+int smla_selftest_wait_timeout(void* workspace, size_t workspace_bytes, uint32_t limit_us,
+                               void* stream);
 
 /*
  * Synchronizes `stream`, then reads the device status word that the last

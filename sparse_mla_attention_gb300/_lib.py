@@ -31,12 +31,14 @@ SMLA_ERR_INDEX = 11
 SMLA_ERR_TIMEOUT = 12
 SMLA_ERR_SINK = 13
 SMLA_ERR_ARG = 14
+SMLA_ERR_DEVICE = 15
 
 SMLA_OP_FWD, SMLA_OP_BWD, SMLA_OP_CSR, SMLA_OP_BWD_HOST = 0, 1, 2, 3
 
 EXPORTED = ("smla_workspace_size", "smla_fwd", "smla_bwd", "smla_bwd_host", "smla_csr_build",
             "smla_get_device_status", "smla_status_string", "smla_version",
-            "smla_profiling", "smla_profile_read", "smla_dsink_static")
+            "smla_profiling", "smla_profile_read", "smla_dsink_static",
+            "smla_selftest_wait_timeout")
 
 
 class SmlaDims(ctypes.Structure):
@@ -83,6 +85,7 @@ def load(path: str = LIB_PATH):
         lib.smla_csr_build.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, sz, vp]
         lib.smla_get_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
         lib.smla_dsink_static.argtypes = [vp] * 5 + [i32, i32, vp]
+        lib.smla_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_uint32, vp]
         lib.smla_profiling.argtypes = [ctypes.c_int]
         lib.smla_profile_read.argtypes = [ctypes.POINTER(SmlaPhaseStat), ctypes.c_int,
                                           ctypes.POINTER(ctypes.c_int)]
@@ -90,7 +93,7 @@ def load(path: str = LIB_PATH):
         lib.smla_status_string.restype = ctypes.c_char_p
         for name in ("smla_workspace_size", "smla_fwd", "smla_bwd", "smla_bwd_host", "smla_csr_build",
                      "smla_get_device_status", "smla_version", "smla_profiling",
-                     "smla_profile_read", "smla_dsink_static"):
+                     "smla_profile_read", "smla_dsink_static", "smla_selftest_wait_timeout"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib

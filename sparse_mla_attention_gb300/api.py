@@ -143,6 +143,9 @@ def sparse_mla_bwd(q: torch.Tensor, kv: torch.Tensor, do: torch.Tensor, o: torch
         _need(sink, "sink", torch.float32, 1)
         if sink.shape[0] != H:
             raise ValueError("sink must have shape [H]")
+    for name, t in (("kv", kv), ("do", do), ("o", o), ("lse", lse), ("topk", topk), ("sink", sink)):
+        if t is not None and t.device != q.device:
+            raise ValueError(f"{name} must be on {q.device}, got {t.device}")
     dims = make_dims(T, H, topk.shape[1], kv.shape[0], r_chunk or 0, scale, D)
     ws = (workspace or Workspace(q.device)).get(workspace_size(SMLA_OP_BWD, dims))
     if out is None:
@@ -151,6 +154,19 @@ def sparse_mla_bwd(q: torch.Tensor, kv: torch.Tensor, do: torch.Tensor, o: torch
         d_sink = None if sink is None else torch.empty(H, dtype=torch.float32, device=q.device)
     else:
         dq, dkv, d_sink = out
+        _need(dq, "dq", torch.bfloat16, 3)
+        _need(dkv, "dkv", torch.bfloat16, 2)
+        if tuple(dq.shape) != (T, H, D) or tuple(dkv.shape) != tuple(kv.shape):
+            raise ValueError("out must be (dq [T,H,D], dkv [num_kv,D], d_sink [H] or None)")
+        if (d_sink is None) != (sink is None):
+            raise ValueError("out's d_sink must be given exactly when sink is given")
+        if d_sink is not None:
+            _need(d_sink, "d_sink", torch.float32, 1)
+            if d_sink.shape[0] != H:
+                raise ValueError("d_sink must have shape [H]")
+        for name, t in (("dq", dq), ("dkv", dkv), ("d_sink", d_sink)):
+            if t is not None and t.device != q.device:
+                raise ValueError(f"{name} must be on {q.device}, got {t.device}")
     _lib.check(_lib.load().smla_bwd(_ptr(q), _ptr(kv), _ptr(do), _ptr(o), _ptr(lse), _ptr(topk),
                                     _ptr(sink), _ptr(dq), _ptr(dkv), _ptr(d_sink),
                                     ctypes.byref(dims), _ptr(ws), ws.numel(), _stream(q.device)),

@@ -89,9 +89,10 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
-                                              volatile int* abort_flag, unsigned* status) {
+                                              volatile int* abort_flag, unsigned* status,
+                                              uint64_t limit_ns = kWaitNs) {
     if (*abort_flag) return false;
-    if (mbar_wait(bar, parity, kWaitNs)) return true;
+    if (mbar_wait(bar, parity, limit_ns)) return true;
     *abort_flag = 1;
     flag_status(status, SMLA_ERR_TIMEOUT);
     return false;
@@ -857,6 +858,43 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
     }
 }
 
+// ============================================================ wait self-test
+// One CTA of four warps runs the unwind path of the kernels above on purpose:
+// warp 0 holds 32 TMEM columns, thread 32 waits (wait_or_abort) on an
+// mbarrier that nothing arrives on, with a limit of `limit_ns`; the wait runs
+// out, sets SMLA_ERR_TIMEOUT and the abort flag; warps 2-3 stand for the other
+// roles and leave their loop when they see the flag (each of their waits is
+// bounded too); then TMEM is freed. No copy or MMA is issued, so nothing is in
+// flight when the CTA exits.
+__global__ void __launch_bounds__(128, 1) wait_selftest_kernel(unsigned* status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tbase;
+    __shared__ volatile int abort_flag;
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) { tmem_alloc(&tbase, 32); tmem_relinquish(); }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x == 32) {
+        wait_or_abort(&bar, 0, &abort_flag, status, limit_ns);
+    } else if (warp >= 2) {
+        // other roles: poll the flag, each poll a bounded wait of its own
+        const uint64_t t0 = globaltimer_ns();
+        while (!abort_flag && globaltimer_ns() - t0 < 4 * limit_ns) __nanosleep(1000);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 32);
+    }
+}
+
 // ================================================================= launchers
 int sm_count() {
     static int cached[64];
@@ -956,6 +994,12 @@ extern "C" int smla_trace_copy(unsigned long long* host, size_t count) {
         case 128: return FN<128>(a, s);        \
         default: return cudaErrorInvalidValue; \
     }
+
+cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t s) {
+    wait_selftest_kernel<<<1, 128, 0, s>>>(status, limit_ns);
+    note_launch();
+    return cudaGetLastError();
+}
 
 cudaError_t launch_attn_sdi(const ChunkArgs& a, cudaStream_t s) {
     if (a.T == 0) return cudaSuccess;

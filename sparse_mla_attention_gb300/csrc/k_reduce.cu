@@ -75,30 +75,40 @@ cudaError_t launch_delta(const uint16_t* o, const uint16_t* dO, float* delta,
 }
 
 // ------------------------------------------------------------------ d_sink
-// One block per head. Thread i sums tokens i, i+256, ... in ascending order,
-// then a fixed shared-memory tree combines the 256 partials: the order of
-// every addition is fixed, so the result is bitwise reproducible.
+// One block of 8 warps per head. Thread i sums tokens i, i+256, ... in
+// ascending order; each warp then combines its 32 partials with a butterfly
+// of shuffles, and warp 0 combines the 8 warp sums the same way. Every
+// addition has a fixed place in that tree, so the result is bitwise
+// reproducible.
 // Term: the sink's softmax weight exp(sink_h - lse) times (0 - delta), the
 // sink having no value row.
+__device__ __forceinline__ float warp_sum_fixed(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
 __global__ void __launch_bounds__(256) dsink_kernel(const float* __restrict__ delta,
                                                     const float* __restrict__ lse,
                                                     const float* __restrict__ sink,
                                                     float* __restrict__ d_sink, int T, int H) {
-    __shared__ float part[256];
+    __shared__ float warp_part[8];
     const int h = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float sh = sink[h];
     float acc = 0.f;
     for (int t = threadIdx.x; t < T; t += 256) {
         const float l = lse[int64_t(t) * H + h];
         acc -= expf(sh - l) * delta[int64_t(t) * H + h];
     }
-    part[threadIdx.x] = acc;
+    acc = warp_sum_fixed(acc);
+    if (lane == 0) warp_part[warp] = acc;
     __syncthreads();
-    for (int w = 128; w > 0; w >>= 1) {
-        if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
-        __syncthreads();
+    if (warp == 0) {
+        float v = lane < 8 ? warp_part[lane] : 0.f;
+        v = warp_sum_fixed(v);
+        if (lane == 0) d_sink[h] = v;
     }
-    if (threadIdx.x == 0) d_sink[h] = part[0];
 }
 
 cudaError_t launch_dsink(const float* delta, const float* lse, const float* sink,

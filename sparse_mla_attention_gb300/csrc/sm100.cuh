@@ -1,6 +1,6 @@
 // sm100.cuh -- thin inline-PTX wrappers for the Blackwell (sm_100 family,
 // here sm_103a) features the tensor-core kernels use: mbarriers with bounded
-// waits, TMA (tiled and 4-row gather), tcgen05 tensor-memory allocation, MMA,
+// waits, TMA (tiled loads and stores), tcgen05 tensor-memory allocation, MMA,
 // commit, loads and stores, and the shared-memory / instruction descriptors.
 // Written from the public PTX ISA description of these instructions.
 #pragma once
@@ -71,10 +71,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
 }
 
 // ----------------------------------------------------------------------- TMA
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
-}
-
 // 2-D tiled load of one box at (x = inner element index, y = row) into smem,
 // completing `bytes` of transaction count on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int x, int y,
@@ -113,18 +109,6 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 // Waits until all committed bulk stores have completed.
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// 2-D gather of four rows (y0..y3) of one box width starting at column x;
-// the tensor map's box is one row high. The four rows land contiguously.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, int x, int y0, int y1,
-                                            int y2, int y3, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
-        "r"(smem_u32(bar))
-        : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -261,22 +245,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// Named barrier among `count` threads (a multiple of 32) of the CTA.
-__device__ __forceinline__ void named_bar(uint32_t id, uint32_t count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Each thread of the warp writes 16 consecutive 32-bit columns of its lane.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15])
-        : "memory");
-}
-
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor, 128-byte swizzle. Tiles are stored as
 // 8-row x 128-byte swizzle atoms (1024 B, 1024-byte aligned).
@@ -300,14 +268,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
            | (1u << 10)                      // B: bf16
            | (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
            (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
-}
-
-// Byte offset of element (row, col) of a bf16 tile stored as consecutive
-// 128-byte rows with the 128-byte swizzle (the layout TMA writes for a
-// 64-column box with CU_TENSOR_MAP_SWIZZLE_128B).
-__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
-    const uint32_t chunk = (col >> 3) ^ (row & 7u);
-    return row * 128u + chunk * 16u + (col & 7u) * 2u;
 }
 
 }  // namespace sm100

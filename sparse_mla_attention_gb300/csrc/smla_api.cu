@@ -152,14 +152,43 @@ int check_arch() {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA; }
 
-// A side stream (and two events) per host thread and device, created on first
-// use: the CSR build of a rank chunk (a chain of small kernels that needs only
+}  // namespace
+
+// Every non-NULL pointer must be device memory of the current device (or
+// managed memory): a host pointer handed to a kernel faults the GPU, so it is
+// refused here, before anything is enqueued. Needs a CUDA context, so it runs
+// after the arch check.
+int check_device_ptrs(const void* const* ptrs, int n) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return SMLA_ERR_CUDA; }
+    for (int i = 0; i < n; ++i) {
+        if (!ptrs[i]) continue;
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, ptrs[i]) != cudaSuccess) {
+            cudaGetLastError();
+            return SMLA_ERR_DEVICE;
+        }
+        if (a.type == cudaMemoryTypeManaged) continue;
+        if (a.type != cudaMemoryTypeDevice || a.device != dev) return SMLA_ERR_DEVICE;
+    }
+    return SMLA_OK;
+}
+
+namespace {
+
+// A side stream (and its events) per host thread and device, created on first
+// use. The CSR build of a rank chunk (a chain of small kernels that needs only
 // topk) runs on it, forked from the caller's stream at the start of the chunk
 // and joined back before the chunk's gather, so that it overlaps the delta and
-// attention phases. The caller sees all work ordered on its own stream.
+// attention phases. The dq kernel runs on it too, after the chunk's S/dP/dS
+// kernel, while the dKV gather runs on the caller's stream: dq is bound by the
+// latency of its kv copies and the gather by HBM bandwidth, so the two share
+// the SMs (dq is dispatched first, from the higher-priority stream, and the
+// gather's blocks fill the room beside it). The caller sees all work ordered
+// on its own stream.
 struct SideStream {
     cudaStream_t stream = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, sdi_done = nullptr, dq_done = nullptr;
 };
 
 SideStream* side_stream() {
@@ -174,7 +203,9 @@ SideStream* side_stream() {
         cudaDeviceGetStreamPriorityRange(&lo, &hi);
         if (cudaStreamCreateWithPriority(&ss.stream, cudaStreamNonBlocking, hi) != cudaSuccess ||
             cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+            cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss.sdi_done, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss.dq_done, cudaEventDisableTiming) != cudaSuccess) {
             cudaGetLastError();
             ss = SideStream{};
             return nullptr;
@@ -268,18 +299,24 @@ int enqueue_bwd(const BwdArgs& A, const smla_dims& d, const BwdPlan& plan, char*
                 prof::Scope ph(prof::kSdi, s);
                 if ((rc = cuda_rc(launch_attn_sdi(a, s)))) return rc;
             }
-            if (!plan.full_stash) {
-                prof::Scope ph(prof::kDq, s);
-                if ((rc = cuda_rc(launch_attn_dq(a, s)))) return rc;
-            } else if (last) {
-                // dq over all ranks from the full stash, once
+            // dq on the side stream, after this SDI (dq of earlier token or rank
+            // chunks precede it on that stream, so the dq accumulator keeps its order)
+            if (!plan.full_stash || last) {
                 ChunkArgs b = a;
-                b.r0 = 0; b.R = int(plan.K); b.ds_off = 0;
-                b.first_chunk = b.last_chunk = true; b.dq_acc = nullptr;
-                prof::Scope ph(prof::kDq, s);
-                if ((rc = cuda_rc(launch_attn_dq(b, s)))) return rc;
+                if (plan.full_stash) {
+                    // dq over all ranks from the full stash, once
+                    b.r0 = 0; b.R = int(plan.K); b.ds_off = 0;
+                    b.first_chunk = b.last_chunk = true; b.dq_acc = nullptr;
+                }
+                if ((rc = cuda_rc(cudaEventRecord(side->sdi_done, s)))) return rc;
+                if ((rc = cuda_rc(cudaStreamWaitEvent(side->stream, side->sdi_done, 0)))) return rc;
+                {
+                    prof::Scope ph(prof::kDq, side->stream);
+                    if ((rc = cuda_rc(launch_attn_dq(b, side->stream)))) return rc;
+                }
+                if (last && feed &&
+                    (rc = cuda_rc(cudaEventRecord(feed->dq_ready[i], side->stream)))) return rc;
             }
-            if (last && feed && (rc = cuda_rc(cudaEventRecord(feed->dq_ready[i], s)))) return rc;
         }
         if ((rc = cuda_rc(cudaStreamWaitEvent(s, side->join, 0)))) return rc;
         prof::Scope ph(prof::kGather, s);
@@ -291,7 +328,15 @@ int enqueue_bwd(const BwdArgs& A, const smla_dims& d, const BwdPlan& plan, char*
                                    reinterpret_cast<float*>(ws + plan.off_partial), dkv_acc, A.dkv,
                                    first, last, s));
         if (rc) return rc;
+        // the next chunk's SDI rewrites the per-chunk dS^T stash that this dq reads
+        if (!last && !plan.full_stash) {
+            if ((rc = cuda_rc(cudaEventRecord(side->dq_done, side->stream)))) return rc;
+            if ((rc = cuda_rc(cudaStreamWaitEvent(s, side->dq_done, 0)))) return rc;
+        }
     }
+    // the caller's stream waits for the last dq
+    if ((rc = cuda_rc(cudaEventRecord(side->dq_done, side->stream)))) return rc;
+    if ((rc = cuda_rc(cudaStreamWaitEvent(s, side->dq_done, 0)))) return rc;
     if (A.sink) {
         prof::Scope ph(prof::kDsink, s);
         if ((rc = cuda_rc(launch_dsink(delta, A.lse, A.sink, A.d_sink, d.T, d.H, s)))) return rc;
@@ -372,6 +417,7 @@ const char* smla_status_string(int code) {
         case SMLA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
         case SMLA_ERR_SINK: return "d_sink must be given exactly when sink is given";
         case SMLA_ERR_ARG: return "invalid argument (scale must be finite and >= 0)";
+        case SMLA_ERR_DEVICE: return "a pointer that must be device memory is not device memory of the current device";
         default: return "unknown status code";
     }
 }
@@ -415,6 +461,7 @@ int smla_fwd(const uint16_t* q, const uint16_t* kv, const int32_t* topk, const f
         overlaps(Span{workspace, workspace_bytes}, ins[1]))
         return SMLA_ERR_OVERLAP;
     if ((rc = check_arch())) return rc;
+    if ((rc = check_device_ptrs(fptrs, 7))) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned* status = static_cast<unsigned*>(workspace);
     if ((rc = cuda_rc(cudaMemsetAsync(status, 0, sizeof(unsigned), s)))) return rc;
@@ -448,6 +495,7 @@ int smla_bwd(const uint16_t* q, const uint16_t* kv, const uint16_t* dO, const ui
                          {d_sink, d_sink ? size_t(d.H) * 4 : 0}, {workspace, workspace_bytes}};
     if ((rc = check_overlap(outs, 4, ins, 7))) return rc;
     if ((rc = check_arch())) return rc;
+    if ((rc = check_device_ptrs(ptrs, 11))) return rc;
 
     const BwdArgs A{q, kv, dO, o, lse, topk, sink, dq, dkv, d_sink};
     return enqueue_bwd(A, d, plan, static_cast<char*>(workspace), static_cast<cudaStream_t>(stream),
@@ -476,6 +524,8 @@ int smla_bwd_host(const uint16_t* q, const uint16_t* kv, const uint16_t* dO, con
     const Span outs[] = {{dq, thd}, {dkv, kvb}, {d_sink, hb}};
     if ((rc = check_overlap(outs, 3, ins, 7))) return rc;
     if ((rc = check_arch())) return rc;
+    const void* wsp[] = {workspace};
+    if ((rc = check_device_ptrs(wsp, 1))) return rc;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     HostStreams* H = host_streams();
@@ -571,12 +621,30 @@ int smla_csr_build(const int32_t* topk, int32_t T, int32_t topk_w, int32_t r0, i
     int rc = check_overlap(outs, 3, ins, 1);
     if (rc) return rc;
     if ((rc = check_arch())) return rc;
+    const void* cptrs[] = {topk, row_ptr, col, workspace};
+    if ((rc = check_device_ptrs(cptrs, 4))) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(workspace);
     unsigned* status = reinterpret_cast<unsigned*>(ws);
     if ((rc = cuda_rc(cudaMemsetAsync(status, 0, sizeof(unsigned), s)))) return rc;
     return cuda_rc(launch_csr(topk, T, topk_w, r0, r_len, num_kv, row_ptr, col, ws + kStatusBytes,
                               plan, status, s));
+}
+
+int smla_selftest_wait_timeout(void* workspace, size_t workspace_bytes, uint32_t limit_us,
+                               void* stream) {
+    if (!workspace) return SMLA_ERR_NULL;
+    if (!aligned16(workspace)) return SMLA_ERR_ALIGN;
+    if (workspace_bytes < kStatusBytes) return SMLA_ERR_WORKSPACE;
+    if (limit_us < 1 || limit_us > 1000000) return SMLA_ERR_ARG;
+    int rc = check_arch();
+    if (rc) return rc;
+    const void* wsp[] = {workspace};
+    if ((rc = check_device_ptrs(wsp, 1))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned* status = static_cast<unsigned*>(workspace);
+    if ((rc = cuda_rc(cudaMemsetAsync(status, 0, sizeof(unsigned), s)))) return rc;
+    return cuda_rc(launch_wait_selftest(status, uint64_t(limit_us) * 1000u, s));
 }
 
 int smla_profiling(int enable) {

@@ -43,6 +43,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Returns SMLA_OK if every non-NULL pointer of `ptrs` is device memory of the
+// current device (or managed memory), else SMLA_ERR_DEVICE (SMLA_ERR_CUDA if
+// the device cannot be queried).
+int check_device_ptrs(const void* const* ptrs, int n);
+
 // ------------------------------------------------------------ workspace plans
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -139,6 +144,9 @@ struct ChunkArgs {
 // The two tensor-core kernels of one chunk: S/dP/P/dS + interm (+ dS stash),
 // then dq from the stash. launch_attn_dq must follow launch_attn_sdi.
 cudaError_t launch_attn_sdi(const ChunkArgs& a, cudaStream_t s);
+// One CTA whose bounded mbarrier wait (limit_ns) runs out on purpose: sets
+// SMLA_ERR_TIMEOUT in `status` through the kernels' own unwind path.
+cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_attn_dq(const ChunkArgs& a, cudaStream_t s);
 
 }  // namespace smla

@@ -13,6 +13,9 @@
 // calls whose kernels overlap on the GPU race; serialize them (one stream, or
 // events between streams). Every call overwrites the T * H entries it reads,
 // so nothing needs clearing between calls.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "smla_internal.cuh"
@@ -28,23 +31,59 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-float* g_static_delta_addr[kMaxDevices];   // device address of g_static_delta, per device
+// Per device: the device address of g_static_delta and the id of the CUDA
+// context it was looked up in. A device address belongs to one context: after
+// cudaDeviceReset the device gets a new context (with a new id), the module is
+// loaded again and the array may sit elsewhere, so the lookup is redone.
+struct StaticAddr {
+    unsigned long long ctx_id;
+    float* addr;
+};
+StaticAddr g_static_delta_addr[kMaxDevices];
+
+// The current context's unique id (never reused within a process), through
+// the driver entry points; false if it cannot be read.
+bool current_ctx_id(unsigned long long* id) {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    if (!get_current || !get_id) {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 4000, cudaEnableDefault, &qa) !=
+                cudaSuccess || qa != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) !=
+                cudaSuccess || qb != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(a);
+        get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(b);
+    }
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 // In host code `g_static_delta` names a host-side shadow, not device memory;
-// the device address must be looked up once per device, with that device
-// current. Returns nullptr on failure.
+// the device address is looked up with the device current, once per device
+// and context. Returns nullptr on failure.
 float* static_delta_for(int dev) {
     if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    unsigned long long ctx = 0;
+    if (!current_ctx_id(&ctx)) return nullptr;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_static_delta_addr[dev]) {
+    StaticAddr& e = g_static_delta_addr[dev];
+    if (!e.addr || e.ctx_id != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_delta) != cudaSuccess) {
             cudaGetLastError();
             return nullptr;
         }
-        g_static_delta_addr[dev] = static_cast<float*>(p);
+        e.addr = static_cast<float*>(p);
+        e.ctx_id = ctx;
     }
-    return g_static_delta_addr[dev];
+    return e.addr;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -79,6 +118,8 @@ extern "C" int smla_dsink_static(const uint16_t* dO, const uint16_t* o, const fl
         return SMLA_ERR_CUDA;
     }
     if (major != 10 || minor != 3) return SMLA_ERR_ARCH;
+    const void* dptrs[] = {dO, o, lse, sink, d_sink};
+    if (const int rc = smla::check_device_ptrs(dptrs, 5)) return rc;
     float* delta = static_delta_for(dev);
     if (!delta) return SMLA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

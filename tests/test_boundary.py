@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.smla_version() == 100
-    for code in range(0, 15):
+    for code in range(0, 16):
         s = lib.smla_status_string(code)
         assert s and s != b"unknown status code"
     assert lib.smla_status_string(999) == b"unknown status code"

@@ -4,7 +4,8 @@ Some callers cannot allocate device memory (another allocator owns it all,
 or allocating is not allowed where they run), so they cannot pass smla_bwd a
 workspace. smla_dsink_static serves them with its scratch in a static device
 array. This test calls it through the C ABI twice in a row and checks both
-results against the d_sink of smla_bwd on the same inputs.
+results against the fp64 oracle (at the parity bar) and, bit for bit,
+against the d_sink of smla_bwd on the same inputs (same kernels).
 
 The file name sorts last so that a run stopping at its first failure has
 already run every other test; it also passes alone in a fresh process.
@@ -16,25 +17,15 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import compare
+from gpu_helpers import Case, compare, to_f64
 
 pytestmark = pytest.mark.gpu
 
 
-def _inputs():
-    import sparse_mla_attention_gb300 as smla
+def _case():
     from sparse_mla_attention_gb300 import workloads as W
-    spec = W.WORKLOADS["t1024_h64"]
-    inp = W.make_inputs(spec)
-
-    def dev_bf16(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
-
-    q, kv, do = (dev_bf16(inp[k]) for k in ("q", "kv", "do"))
-    topk = torch.from_numpy(inp["topk"]).cuda()
-    sink = torch.from_numpy(inp["sink"]).cuda()
-    o, lse = smla.sparse_mla_fwd(q, kv, topk, sink)
-    return q, kv, do, o, lse, topk, sink
+    # O and lse come from the oracle's forward (never from the CUDA path)
+    return Case(W.make_inputs(W.WORKLOADS["t1024_h64"]))
 
 
 def _call_static(lib, do, o, lse, sink, d_sink, T, H):
@@ -43,22 +34,26 @@ def _call_static(lib, do, o, lse, sink, d_sink, T, H):
     return lib.smla_dsink_static(p(do), p(o), p(lse), p(sink), p(d_sink), T, H, stream)
 
 
-def test_static_dsink_matches_bwd_twice():
+def test_static_dsink_matches_oracle_and_bwd_twice():
     from sparse_mla_attention_gb300 import _lib, build
     build.build()
     import sparse_mla_attention_gb300 as smla
     lib = _lib.load()
-    q, kv, do, o, lse, topk, sink = _inputs()
-    T, H, _ = q.shape
-    _, _, ref = smla.sparse_mla_bwd(q, kv, do, o, lse, topk, sink)
+    c = _case()
+    T, H = c.T, c.H
+    _, _, from_bwd = smla.sparse_mla_bwd(c.q, c.kv, c.do, c.o, c.lse, c.topk, c.sink)
+    ref = c.ref_dsink()
     outs = []
     for _ in range(2):
         d_sink = torch.full((H,), float("nan"), device="cuda")
-        assert _call_static(lib, do, o, lse, sink, d_sink, T, H) == _lib.SMLA_OK
+        assert _call_static(lib, c.do, c.o, c.lse, c.sink, d_sink, T, H) == _lib.SMLA_OK
         torch.cuda.synchronize()
         outs.append(d_sink)
     for d_sink in outs:
-        compare("d_sink (static)", d_sink.double().cpu().numpy(), ref.double().cpu().numpy())
+        # against the fp64 oracle, at the bar of every parity test
+        compare("d_sink (static)", to_f64(d_sink), ref)
+        # the same kernels on the same inputs as smla_bwd's d_sink: equal bit for bit
+        assert torch.equal(d_sink, from_bwd)
     assert torch.equal(outs[0], outs[1])
 
 
