@@ -48,11 +48,11 @@ namespace {
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
+}  // namespace
+#ifdef SMLA_TRACE
 // Optional phase timestamps (compiled only with -DSMLA_TRACE; the library
 // build leaves them out): per kernel, CTA (< 8) and item (< 8), 64 events.
 constexpr int kTraceCtas = 8, kTraceItems = 8, kTraceEvents = 64;
-}  // namespace
-#ifdef SMLA_TRACE
 __device__ unsigned long long g_smla_trace[2 * kTraceCtas * kTraceItems * kTraceEvents];
 // per kernel and CTA (< 1024): start and end time of the CTA's MMA thread
 __device__ unsigned long long g_smla_cta_span[2 * 1024 * 3];
@@ -135,6 +135,12 @@ struct SdiParams {
 
 struct SdiShared {
     uint64_t full[8], empty[8];
+    // kempty[s]: one phase per use of slot s that is followed (kSlots uses
+    // later) by a use the copy warps fill, so the copy warps, who skip the
+    // B-stage uses, wait on it for every fill of theirs exactly once, in order
+    // (a parity wait on `empty`, which advances on every use, could see the
+    // slot two phases on and pass too early)
+    uint64_t kempty[8];
     uint64_t s_full, p_ready, x_full[2], x_empty[2], b_done[2], drain;
     uint32_t tbase;
     volatile int abort_flag;
@@ -175,7 +181,11 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 
     if (threadIdx.x == 0) {
         // full: the TMA thread's arrive (with the q / dO bytes) + 64 copy threads
-        for (int s = 0; s < C::kSlots; ++s) { mbar_init(&sh.full[s], 65); mbar_init(&sh.empty[s], 1); }
+        for (int s = 0; s < C::kSlots; ++s) {
+            mbar_init(&sh.full[s], 65);
+            mbar_init(&sh.empty[s], 1);
+            mbar_init(&sh.kempty[s], 1);
+        }
         mbar_init(&sh.s_full, 1);
         mbar_init(&sh.p_ready, 8);
         for (int g = 0; g < 2; ++g) {
@@ -277,11 +287,17 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             for (int k = 0; k + 1 < 8; ++k) pend[k] = pend[k + 1];
             --npend;
         };
+        int use = 0;              // this CTA's ring use index
+        uint32_t kph = 0;         // per slot: parity of its next kempty phase
         for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
             const int pr = item % p.npairs;
             const int ntiles = pr == p.npairs - 1 ? p.tiles_last : 2;
-            for (int c = 0; c < 8; ++c) {
-                if (lane == 0) ok = wait_or_abort(&sh.empty[slot], phase ^ 1u, &sh.abort_flag, p.status);
+            for (int c = 0; c < 8; ++c, ++use) {
+                if (use >= C::kSlots) {   // the slot's previous use must be consumed
+                    if (lane == 0)
+                        ok = wait_or_abort(&sh.kempty[slot], (kph >> slot) & 1u, &sh.abort_flag, p.status);
+                    kph ^= 1u << slot;
+                }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
                 uint8_t* kvb = slots + slot * C::kSlotBytes + 2 * C::kQBytes;
@@ -307,7 +323,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 advance(slot, phase, C::kSlots);
             }
             // the B-stage uses of the ring are signalled by the TMA thread
-            for (int k = 8; k < C::kUses; ++k) advance(slot, phase, C::kSlots);
+            for (int k = 8; k < C::kUses; ++k, ++use) advance(slot, phase, C::kSlots);
 #pragma unroll
             for (int i = 0; i < 32; ++i) idx_cur[i] = idx_nxt[i];
         }
@@ -351,6 +367,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                                    sdesc_sw128(sb + k * 32, 16, 1024), C::kIdescA, (c | k) != 0);
                     }
                     mma_commit(&sh.empty[slot]);
+                    if ((c + C::kSlots) % C::kUses < 8) mma_commit(&sh.kempty[slot]);
                     advance(slot, phase, C::kSlots);
                 }
                 if (!ok) break;
@@ -390,6 +407,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                         ++x_uses[g];
                     }
                     mma_commit(&sh.empty[slot]);
+                    if ((8 + c + C::kSlots) % C::kUses < 8) mma_commit(&sh.kempty[slot]);
                     advance(slot, phase, C::kSlots);
                 }
                 if (!ok) break;

@@ -32,9 +32,10 @@
 // Shared memory: a ring of five 32 KB kv slots (an S-stage use holds 256 rank
 // rows x 64 columns, an O-stage use 128 rank rows x 128 columns as two
 // 64-column blocks), three 16 KB q buffers and four 4 KB staging tiles. Uses
-// are numbered across the CTA's tokens; use g sits in slot g % 5. Copy team k
-// (four warps) fills the uses g = k, k + 2, ...: two teams, because more
-// copies in flight per SM made every copy slower (measured with 1 to 5 teams).
+// are numbered across the CTA's tokens; copy team k (four warps) fills the
+// uses g = k, k + 2, ... in slots of its own (team 0: slots 0-2, team 1: slots
+// 3-4; see ft_slot): two teams, because more copies in flight per SM made
+// every copy slower (measured with 1 to 5 teams).
 // The next token's q is prefetched into L2 while the current one runs.
 // Every mbarrier wait is bounded; a timeout sets SMLA_ERR_TIMEOUT, stops the
 // CTA's loops, waits (bounded) for its own copies and MMAs and frees TMEM.
@@ -52,6 +53,20 @@ constexpr float kFtLog2e = 1.4426950408889634f;
 constexpr int kFtSlots = 5;
 constexpr int kFtSlotBytes = 32768;
 constexpr int kFtTeams = 2;
+
+// Kv use g is filled by copy team g % kFtTeams, which owns a fixed set of
+// slots and fills them in turn: every slot is filled by one team only, in the
+// order the MMA consumes it, so a team waiting for a slot is never more than
+// one phase of that slot's empty barrier ahead (a parity wait cannot tell two
+// phases apart). With 5 slots, team 0 owns slots 0-2 and team 1 slots 3-4.
+__device__ __forceinline__ void ft_slot(int g, int& slot, uint32_t& phase) {
+    const int team = g % kFtTeams, i = g / kFtTeams;
+    const int base = kFtSlots / kFtTeams, extra = kFtSlots % kFtTeams;
+    const int n = base + (team < extra ? 1 : 0);
+    const int first = team * base + (team < extra ? team : extra);
+    slot = first + i % n;
+    phase = uint32_t(i / n) & 1u;
+}
 constexpr int kFtTeamWarps = 4;
 constexpr int kFtEpiWarps = 8;                                     // two per TMEM lane quarter
 constexpr int kFtCopyWarp0 = 2 + kFtEpiWarps;
@@ -232,8 +247,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             int n0, n1;
             load_use(g + kFtTeams, n0, n1);
             const int c0 = ft_row_of(raw0, p.N, bad), c1 = ft_row_of(raw1, p.N, bad);
-            const int slot = g % kFtSlots;
-            const uint32_t ph = uint32_t(g / kFtSlots) & 1u;
+            int slot; uint32_t ph;
+            ft_slot(g, slot, ph);
             bool ok = true;
             if (lane == 0) ok = ft_wait(&sh.empty[slot], ph ^ 1u, &sh.abort_flag, p.status);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -289,8 +304,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                     if (!ok) break;
                     const uint32_t qa = smem_u32(qbuf + b * kFtQBytes);
                     for (int j = 0; j < nt2 && ok; ++j, ++g) {
-                        const int slot = g % kFtSlots;
-                        ok = ft_wait(&sh.full[slot], uint32_t(g / kFtSlots) & 1u, &sh.abort_flag, p.status);
+                        int slot; uint32_t ph;
+                        ft_slot(g, slot, ph);
+                        ok = ft_wait(&sh.full[slot], ph, &sh.abort_flag, p.status);
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t sb = smem_u32(ring + slot * kFtSlotBytes);
@@ -316,8 +332,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                     if (!ok) break;
                     tc_fence_after();
                     for (int j = 0; j < nt && ok; ++j, ++g) {
-                        const int slot = g % kFtSlots;
-                        ok = ft_wait(&sh.full[slot], uint32_t(g / kFtSlots) & 1u, &sh.abort_flag, p.status);
+                        int slot; uint32_t ph;
+                        ft_slot(g, slot, ph);
+                        ok = ft_wait(&sh.full[slot], ph, &sh.abort_flag, p.status);
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t sb = smem_u32(ring + slot * kFtSlotBytes);
