@@ -142,6 +142,40 @@ int smla_bwd(const uint16_t* q, const uint16_t* kv, const uint16_t* dO,
              void* stream);
 
 /*
+ * One rank's share of a token-sharded backward (several GPUs, each holding a
+ * slice of the tokens; the RL-Kernel page's "Algorithmic arrangements" item 5:
+ * partials combined in a fixed rank order, the collective used only to move
+ * them). Same arguments, layouts and errors as smla_bwd for the rank's T
+ * tokens, except the kv gradient and d_sink are left as fp32 partial sums over
+ * these tokens, unrounded:
+ *   dkv_partial [num_kv, D] fp32 = sum over this rank's (t, h, r) of the dkv terms;
+ *   d_sink_partial [H] fp32 (NULL iff sink is NULL) = -sum over this rank's t of
+ *   exp(sink - lse) * delta.
+ * dq of the rank's tokens is final (bf16). Every rank passes the full kv and
+ * gathers the others' partials; smla_reduce_partials then adds them in rank
+ * order and rounds once.
+ */
+int smla_bwd_partial(const uint16_t* q, const uint16_t* kv, const uint16_t* dO,
+                     const uint16_t* o, const float* lse, const int32_t* topk,
+                     const float* sink, uint16_t* dq, float* dkv_partial,
+                     float* d_sink_partial, const smla_dims* dims, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
+ * Ordered sum of n_parts partials (the combine step of a token-sharded
+ * backward): for every i in [0, n),
+ *   s = partials[0][i] + partials[1][i] + ... + partials[n_parts - 1][i]
+ * added left to right in fp32, so every rank that runs it on the same gathered
+ * partials gets the same bits. Writes s rounded to bf16 (RNE) to out_bf16
+ * and / or s to out_f32 (either may be NULL, not both).
+ *   partials [n_parts, n] fp32 (contiguous, device); n a multiple of 4.
+ * Errors: SMLA_ERR_NULL, SMLA_ERR_SHAPE (n_parts < 1, n < 0 or not a
+ * multiple of 4), SMLA_ERR_ALIGN, SMLA_ERR_OVERLAP, SMLA_ERR_DEVICE.
+ */
+int smla_reduce_partials(const float* partials, int32_t n_parts, int64_t n,
+                         uint16_t* out_bf16, float* out_f32, void* stream);
+
+/*
  * The same backward with every input and output in HOST memory (the pages
  * have no such call; it is the end-to-end form of smla_bwd). Arguments,
  * results and errors are those of smla_bwd, except that q, kv, dO, o, lse,

@@ -38,7 +38,7 @@ SMLA_OP_FWD, SMLA_OP_BWD, SMLA_OP_CSR, SMLA_OP_BWD_HOST = 0, 1, 2, 3
 EXPORTED = ("smla_workspace_size", "smla_fwd", "smla_bwd", "smla_bwd_host", "smla_csr_build",
             "smla_get_device_status", "smla_status_string", "smla_version",
             "smla_profiling", "smla_profile_read", "smla_dsink_static",
-            "smla_selftest_wait_timeout")
+            "smla_selftest_wait_timeout", "smla_bwd_partial", "smla_reduce_partials")
 
 
 class SmlaDims(ctypes.Structure):
@@ -82,6 +82,8 @@ def load(path: str = LIB_PATH):
         lib.smla_fwd.argtypes = [vp] * 6 + [dims_p, vp, sz, vp]
         lib.smla_bwd.argtypes = [vp] * 10 + [dims_p, vp, sz, vp]
         lib.smla_bwd_host.argtypes = [vp] * 10 + [dims_p, vp, sz, vp]
+        lib.smla_bwd_partial.argtypes = [vp] * 10 + [dims_p, vp, sz, vp]
+        lib.smla_reduce_partials.argtypes = [vp, i32, ctypes.c_int64, vp, vp, vp]
         lib.smla_csr_build.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, sz, vp]
         lib.smla_get_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
         lib.smla_dsink_static.argtypes = [vp] * 5 + [i32, i32, vp]
@@ -93,7 +95,8 @@ def load(path: str = LIB_PATH):
         lib.smla_status_string.restype = ctypes.c_char_p
         for name in ("smla_workspace_size", "smla_fwd", "smla_bwd", "smla_bwd_host", "smla_csr_build",
                      "smla_get_device_status", "smla_version", "smla_profiling",
-                     "smla_profile_read", "smla_dsink_static", "smla_selftest_wait_timeout"):
+                     "smla_profile_read", "smla_dsink_static", "smla_selftest_wait_timeout",
+                     "smla_bwd_partial", "smla_reduce_partials"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib

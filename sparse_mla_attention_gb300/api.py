@@ -178,6 +178,70 @@ def sparse_mla_bwd(q: torch.Tensor, kv: torch.Tensor, do: torch.Tensor, o: torch
     return dq, dkv, d_sink
 
 
+def sparse_mla_bwd_partial(q: torch.Tensor, kv: torch.Tensor, do: torch.Tensor, o: torch.Tensor,
+                           lse: torch.Tensor, topk: torch.Tensor, sink: Optional[torch.Tensor] = None,
+                           scale: Optional[float] = None, r_chunk: Optional[int] = None,
+                           workspace: Optional[Workspace] = None, check_status: bool = True):
+    """One rank's share of a token-sharded backward (smla_bwd_partial).
+
+    q, do, o, lse, topk hold this rank's tokens; kv (and sink) are the full
+    tensors. Returns (dq [T,H,512] bf16, dkv_partial [num_kv,512] fp32,
+    d_sink_partial [H] fp32 or None): the kv and sink gradients summed over
+    this rank's tokens only, unrounded.
+    """
+    _need(q, "q", torch.bfloat16, 3)
+    _need(kv, "kv", torch.bfloat16, 2)
+    _need(do, "do", torch.bfloat16, 3)
+    _need(o, "o", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    _need(topk, "topk", torch.int32, 2)
+    T, H, D = q.shape
+    if do.shape != q.shape or o.shape != q.shape:
+        raise ValueError("do and o must have the shape of q")
+    if tuple(lse.shape) != (T, H):
+        raise ValueError("lse must have shape [T, H]")
+    if kv.shape[1] != D or topk.shape[0] != T:
+        raise ValueError("shape mismatch between q, kv and topk")
+    if sink is not None:
+        _need(sink, "sink", torch.float32, 1)
+        if sink.shape[0] != H:
+            raise ValueError("sink must have shape [H]")
+    for name, t in (("kv", kv), ("do", do), ("o", o), ("lse", lse), ("topk", topk), ("sink", sink)):
+        if t is not None and t.device != q.device:
+            raise ValueError(f"{name} must be on {q.device}, got {t.device}")
+    dims = make_dims(T, H, topk.shape[1], kv.shape[0], r_chunk or 0, scale, D)
+    ws = (workspace or Workspace(q.device)).get(workspace_size(SMLA_OP_BWD, dims))
+    dq = torch.empty_like(q)
+    dkv = torch.empty(kv.shape, dtype=torch.float32, device=q.device)
+    d_sink = None if sink is None else torch.empty(H, dtype=torch.float32, device=q.device)
+    _lib.check(_lib.load().smla_bwd_partial(_ptr(q), _ptr(kv), _ptr(do), _ptr(o), _ptr(lse),
+                                            _ptr(topk), _ptr(sink), _ptr(dq), _ptr(dkv),
+                                            _ptr(d_sink), ctypes.byref(dims), _ptr(ws), ws.numel(),
+                                            _stream(q.device)),
+               "smla_bwd_partial")
+    if check_status:
+        st = device_status(ws)
+        if st != _lib.SMLA_OK:
+            raise _lib.SmlaError(st, "smla_bwd_partial (device)")
+    return dq, dkv, d_sink
+
+
+def reduce_partials(partials: torch.Tensor, want_bf16: bool = True, want_f32: bool = False):
+    """Ordered sum over the first dimension of partials [n_parts, n] fp32
+    (smla_reduce_partials): parts added in index order, in fp32.
+    Returns (sum rounded to bf16 or None, fp32 sum or None)."""
+    _need(partials, "partials", torch.float32, 2)
+    if not (want_bf16 or want_f32):
+        raise ValueError("ask for a bf16 or an fp32 result")
+    n_parts, n = partials.shape
+    out_b = torch.empty(n, dtype=torch.bfloat16, device=partials.device) if want_bf16 else None
+    out_f = torch.empty(n, dtype=torch.float32, device=partials.device) if want_f32 else None
+    _lib.check(_lib.load().smla_reduce_partials(_ptr(partials), int(n_parts), int(n), _ptr(out_b),
+                                                _ptr(out_f), _stream(partials.device)),
+               "smla_reduce_partials")
+    return out_b, out_f
+
+
 def _need_host(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")

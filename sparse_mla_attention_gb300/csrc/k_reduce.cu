@@ -118,6 +118,42 @@ cudaError_t launch_dsink(const float* delta, const float* lse, const float* sink
     return cudaGetLastError();
 }
 
+// --------------------------------------------------------- ordered partials
+// The combine step of a token-sharded backward: every element is the sum of
+// the ranks' partials taken in rank order (a fixed order, so every rank that
+// runs this on the same gathered partials gets the same bits). One thread per
+// 4 consecutive elements, grid-stride.
+__global__ void __launch_bounds__(256) reduce_partials_kernel(const float4* __restrict__ parts,
+                                                              int n_parts, int64_t n4,
+                                                              uint2* __restrict__ out_bf16,
+                                                              float4* __restrict__ out_f32) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        float4 a = parts[i];
+        for (int r = 1; r < n_parts; ++r) {
+            const float4 v = parts[int64_t(r) * n4 + i];
+            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+        }
+        if (out_f32) out_f32[i] = a;
+        if (out_bf16) out_bf16[i] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+    }
+}
+
+cudaError_t launch_reduce_partials(const float* partials, int n_parts, int64_t n,
+                                   uint16_t* out_bf16, float* out_f32, cudaStream_t s) {
+    const int64_t n4 = n / 4;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t want = (n4 + 255) / 256;
+    const int grid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
+    reduce_partials_kernel<<<grid > 0 ? grid : 1, 256, 0, s>>>(
+        reinterpret_cast<const float4*>(partials), n_parts, n4, reinterpret_cast<uint2*>(out_bf16),
+        reinterpret_cast<float4*>(out_f32));
+    note_launch();
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------ exclusive scan
 // Reduce-then-scan over tiles of 2048 int32 (256 threads x 8): tile sums,
 // then one block scans the tile sums (looping when there are more than

@@ -220,6 +220,7 @@ struct BwdArgs {
     const uint16_t* q; const uint16_t* kv; const uint16_t* dO; const uint16_t* o;
     const float* lse; const int32_t* topk; const float* sink;
     uint16_t* dq; uint16_t* dkv; float* d_sink;
+    float* dkv_f32;   // when set, dkv is written here in fp32, unrounded (dkv unused)
 };
 
 // Optional token pipelining of a call whose inputs arrive in token chunks:
@@ -239,7 +240,11 @@ int enqueue_bwd(const BwdArgs& A, const smla_dims& d, const BwdPlan& plan, char*
     unsigned* status = reinterpret_cast<unsigned*>(ws);
     if ((rc = cuda_rc(cudaMemsetAsync(status, 0, sizeof(unsigned), s)))) return rc;
     if (d.T == 0) {
-        if ((rc = cuda_rc(cudaMemsetAsync(A.dkv, 0, size_t(d.num_kv) * kD * 2, s)))) return rc;
+        if (A.dkv_f32) {
+            if ((rc = cuda_rc(cudaMemsetAsync(A.dkv_f32, 0, size_t(d.num_kv) * kD * 4, s)))) return rc;
+        } else if ((rc = cuda_rc(cudaMemsetAsync(A.dkv, 0, size_t(d.num_kv) * kD * 2, s)))) {
+            return rc;
+        }
         if (A.d_sink) return cuda_rc(cudaMemsetAsync(A.d_sink, 0, size_t(d.H) * 4, s));
         return SMLA_OK;
     }
@@ -250,7 +255,9 @@ int enqueue_bwd(const BwdArgs& A, const smla_dims& d, const BwdPlan& plan, char*
     uint16_t* dsT = reinterpret_cast<uint16_t*>(ws + plan.off_dst);
     float* dq_acc = plan.nchunks > 1 && !plan.full_stash
                         ? reinterpret_cast<float*>(ws + plan.off_dqacc) : nullptr;
-    float* dkv_acc = plan.nchunks > 1 ? reinterpret_cast<float*>(ws + plan.off_dkvacc) : nullptr;
+    // fp32 dkv accumulator across rank chunks; with an fp32 output it is the output
+    float* dkv_acc = A.dkv_f32 ? A.dkv_f32
+                     : plan.nchunks > 1 ? reinterpret_cast<float*>(ws + plan.off_dkvacc) : nullptr;
     const int64_t Hp = pad_heads(d.H);
     const int64_t ds_rows = plan.full_stash ? plan.K : round_up_ranks(int(plan.R));
     const int whole[2] = {0, d.T};
@@ -326,7 +333,7 @@ int enqueue_bwd(const BwdArgs& A, const smla_dims& d, const BwdPlan& plan, char*
                                    reinterpret_cast<int32_t*>(ws + plan.off_segrow),
                                    ws + plan.off_scan_tmp2,
                                    reinterpret_cast<float*>(ws + plan.off_partial), dkv_acc, A.dkv,
-                                   first, last, s));
+                                   first, last && !A.dkv_f32, s));
         if (rc) return rc;
         // the next chunk's SDI rewrites the per-chunk dS^T stash that this dq reads
         if (!last && !plan.full_stash) {
@@ -391,6 +398,43 @@ HostPlan plan_host(const smla_dims& d, const BwdPlan& bp) {
     h.bytes = off;
     return h;
 }
+}  // namespace
+}  // namespace smla
+
+namespace smla {
+namespace {
+
+// Validation and launch shared by smla_bwd (bf16 dkv) and smla_bwd_partial
+// (fp32 dkv, A.dkv_f32). Pointers to zero-size tensors (T == 0) may be NULL.
+int validate_and_enqueue_bwd(const BwdArgs& A, const smla_dims* dims, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    int rc = check_dims(dims, true);
+    if (rc) return rc;
+    const smla_dims& d = *dims;
+    const bool has_tokens = d.T > 0;
+    const void* dkv_out = A.dkv_f32 ? static_cast<const void*>(A.dkv_f32) : A.dkv;
+    const size_t dkv_bytes = size_t(d.num_kv) * kD * (A.dkv_f32 ? 4 : 2);
+    if (!A.kv || !dkv_out || !workspace) return SMLA_ERR_NULL;
+    if (has_tokens && (!A.q || !A.dO || !A.o || !A.lse || !A.topk || !A.dq)) return SMLA_ERR_NULL;
+    if ((A.sink == nullptr) != (A.d_sink == nullptr)) return SMLA_ERR_SINK;
+    const void* ptrs[] = {A.q, A.kv, A.dO, A.o, A.lse, A.topk, A.sink, A.dq, dkv_out, A.d_sink, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SMLA_ERR_ALIGN;
+    const BwdPlan plan = plan_bwd(d);
+    if (workspace_bytes < plan.bytes) return SMLA_ERR_WORKSPACE;
+    const size_t thd = size_t(d.T) * d.H * kD * 2, th4 = size_t(d.T) * d.H * 4;
+    const Span ins[] = {{A.q, thd}, {A.kv, size_t(d.num_kv) * kD * 2}, {A.dO, thd}, {A.o, thd},
+                        {A.lse, th4}, {A.topk, size_t(d.T) * d.topk * 4},
+                        {A.sink, A.sink ? size_t(d.H) * 4 : 0}};
+    const Span outs[] = {{A.dq, thd}, {dkv_out, dkv_bytes},
+                         {A.d_sink, A.d_sink ? size_t(d.H) * 4 : 0}, {workspace, workspace_bytes}};
+    if ((rc = check_overlap(outs, 4, ins, 7))) return rc;
+    if ((rc = check_arch())) return rc;
+    if ((rc = check_device_ptrs(ptrs, 11))) return rc;
+    return enqueue_bwd(A, d, plan, static_cast<char*>(workspace), static_cast<cudaStream_t>(stream),
+                       nullptr);
+}
+
 }  // namespace
 }  // namespace smla
 
@@ -474,32 +518,35 @@ int smla_bwd(const uint16_t* q, const uint16_t* kv, const uint16_t* dO, const ui
              const float* lse, const int32_t* topk, const float* sink, uint16_t* dq,
              uint16_t* dkv, float* d_sink, const smla_dims* dims, void* workspace,
              size_t workspace_bytes, void* stream) {
-    int rc = check_dims(dims, true);
-    if (rc) return rc;
-    const smla_dims& d = *dims;
-    // Pointers to zero-size tensors (T == 0) may be NULL.
-    const bool has_tokens = d.T > 0;
-    if (!kv || !dkv || !workspace) return SMLA_ERR_NULL;
-    if (has_tokens && (!q || !dO || !o || !lse || !topk || !dq)) return SMLA_ERR_NULL;
-    if ((sink == nullptr) != (d_sink == nullptr)) return SMLA_ERR_SINK;
-    const void* ptrs[] = {q, kv, dO, o, lse, topk, sink, dq, dkv, d_sink, workspace};
-    for (const void* p : ptrs)
-        if (p && !aligned16(p)) return SMLA_ERR_ALIGN;
-    const BwdPlan plan = plan_bwd(d);
-    if (workspace_bytes < plan.bytes) return SMLA_ERR_WORKSPACE;
-    const size_t thd = size_t(d.T) * d.H * kD * 2, th4 = size_t(d.T) * d.H * 4;
-    const Span ins[] = {{q, thd}, {kv, size_t(d.num_kv) * kD * 2}, {dO, thd}, {o, thd},
-                        {lse, th4}, {topk, size_t(d.T) * d.topk * 4},
-                        {sink, sink ? size_t(d.H) * 4 : 0}};
-    const Span outs[] = {{dq, thd}, {dkv, size_t(d.num_kv) * kD * 2},
-                         {d_sink, d_sink ? size_t(d.H) * 4 : 0}, {workspace, workspace_bytes}};
-    if ((rc = check_overlap(outs, 4, ins, 7))) return rc;
-    if ((rc = check_arch())) return rc;
-    if ((rc = check_device_ptrs(ptrs, 11))) return rc;
+    const BwdArgs A{q, kv, dO, o, lse, topk, sink, dq, dkv, d_sink, nullptr};
+    return validate_and_enqueue_bwd(A, dims, workspace, workspace_bytes, stream);
+}
 
-    const BwdArgs A{q, kv, dO, o, lse, topk, sink, dq, dkv, d_sink};
-    return enqueue_bwd(A, d, plan, static_cast<char*>(workspace), static_cast<cudaStream_t>(stream),
-                       nullptr);
+int smla_bwd_partial(const uint16_t* q, const uint16_t* kv, const uint16_t* dO, const uint16_t* o,
+                     const float* lse, const int32_t* topk, const float* sink, uint16_t* dq,
+                     float* dkv_partial, float* d_sink_partial, const smla_dims* dims,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+    const BwdArgs A{q, kv, dO, o, lse, topk, sink, dq, nullptr, d_sink_partial, dkv_partial};
+    return validate_and_enqueue_bwd(A, dims, workspace, workspace_bytes, stream);
+}
+
+int smla_reduce_partials(const float* partials, int32_t n_parts, int64_t n, uint16_t* out_bf16,
+                         float* out_f32, void* stream) {
+    if (!partials && n > 0) return SMLA_ERR_NULL;
+    if (!out_bf16 && !out_f32) return SMLA_ERR_NULL;
+    if (n_parts < 1 || n < 0 || n % 4 != 0) return SMLA_ERR_SHAPE;
+    const void* ptrs[] = {partials, out_bf16, out_f32};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SMLA_ERR_ALIGN;
+    const Span ins[] = {{partials, size_t(n_parts) * size_t(n) * 4}};
+    const Span outs[] = {{out_bf16, out_bf16 ? size_t(n) * 2 : 0}, {out_f32, out_f32 ? size_t(n) * 4 : 0}};
+    int rc = check_overlap(outs, 2, ins, 1);
+    if (rc) return rc;
+    if ((rc = check_arch())) return rc;
+    if ((rc = check_device_ptrs(ptrs, 3))) return rc;
+    if (n == 0) return SMLA_OK;
+    return cuda_rc(launch_reduce_partials(partials, n_parts, n, out_bf16, out_f32,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 int smla_bwd_host(const uint16_t* q, const uint16_t* kv, const uint16_t* dO, const uint16_t* o,

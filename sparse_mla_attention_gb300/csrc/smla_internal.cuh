@@ -106,6 +106,10 @@ cudaError_t launch_delta(const uint16_t* o, const uint16_t* dO, float* delta,
                          int64_t rows, cudaStream_t s);
 cudaError_t launch_dsink(const float* delta, const float* lse, const float* sink,
                          float* d_sink, int T, int H, cudaStream_t s);
+// out[i] = partials[0][i] + partials[1][i] + ... + partials[n_parts-1][i], added
+// in that order in fp32 (n a multiple of 4); bf16 (RNE) and / or fp32 outputs.
+cudaError_t launch_reduce_partials(const float* partials, int n_parts, int64_t n,
+                                   uint16_t* out_bf16, float* out_f32, cudaStream_t s);
 cudaError_t launch_exclusive_scan(const int32_t* in, int32_t* out, int64_t n,
                                   void* tmp, cudaStream_t s, bool write_total);
 cudaError_t launch_csr(const int32_t* topk, int T, int topk_w, int r0, int r_len, int num_kv,
