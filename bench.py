@@ -499,14 +499,14 @@ OVERLAPPED_PHASES = ("csr", "attn_dq", "gather")
 # DRAM traffic per launch of the dominant kernels, from one ncu capture (see
 # profiles/), valid only while the kernel source is the one captured.
 _NCU_TRAFFIC = {
-    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "a9366e6493ee301b"),
-                 "bytes_per_token": (141.261568e6 + 274.870272e6) / 512,
+    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "e756570005956a5d"),
+                 "bytes_per_token": (141.009920e6 + 274.377728e6) / 512,
                  "note": "ncu capture of the first 512 tokens, scaled by tokens"},
-    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "a9366e6493ee301b"),
-                "bytes_per_token": (69.764096e6 + 15.354880e6) / 512,
+    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "e756570005956a5d"),
+                "bytes_per_token": (69.773312e6 + 15.686400e6) / 512,
                 "note": "ncu capture of the first 512 tokens, scaled by tokens"},
-    "fwd_tc": {"sources": ("sparse_mla_attention_gb300/csrc/k_fwd_tc.cu", "3275cc58b29baa34"),
-               "bytes_per_token": (72.340224e6 + 16.913664e6) / 512,
+    "fwd_tc": {"sources": ("sparse_mla_attention_gb300/csrc/k_fwd_tc.cu", "9782f171a5790295"),
+               "bytes_per_token": (72.783872e6 + 17.696512e6) / 512,
                "note": "ncu capture of the first 512 tokens, scaled by tokens"},
 }
 
