@@ -11,21 +11,26 @@
 // sdi_kernel (S, dP, P, dS, interm): persistent, one CTA per SM. A work item
 // is (token t, 256 ranks) = two 128-rank tiles.
 //  * A stage: per tile, one MMA stream computes S^T and dP^T together:
-//    M = 128 ranks, N = 2H (the q rows of token t followed by its dO rows),
-//    K = 512, in eight 64-column steps. The kv rows of each step are gathered
-//    by two copy warps (16-byte cp.async through L2); the q / dO tiles come
-//    by TMA.
+//    M = 128 ranks, N = 2H (the q rows of token t and its dO rows, in the
+//    order the two tensors sit in memory), K = 512, in eight 64-column steps.
+//    The kv rows of each step are gathered by two copy warps (16-byte cp.async
+//    through L2); q and dO come by TMA, as one box per step when both tensors
+//    can be addressed as one paired tensor map, else as two.
 //  * Epilogue: each TMEM row (one rank) becomes P and scale*dS, written back
 //    into TMEM as bf16 pairs (the A operand of the next GEMM); scale*dS^T is
-//    also stashed in global memory for the dq kernel (staged, TMA store).
+//    also stashed in global memory for the dq kernel. Results leave TMEM
+//    through registers and a per-warp staging tile, by TMA store.
 //  * B stage: interm = [P | scale*dS] x [dO ; q] with A from TMEM: M = 128
 //    ranks, N = 128 columns of D per step, K = 2H. Each tile has one
-//    128-column accumulator; the tiles alternate so that one tile's drain
-//    (TMEM -> bf16 -> staging -> TMA store) overlaps the other tile's MMAs.
-// TMEM (512 columns): tile g owns columns [256g, 256g + 256): S^T | dP^T in
+//    128-column accumulator; the tiles alternate, and all eight epilogue warps
+//    drain each accumulator (TMEM -> bf16 -> staging tile -> TMA store) while
+//    the other tile's MMAs run.
+//  * Overlap: S^T / dP^T complete per tile; the epilogue warps finish tile 0's
+//    P / dS first, and tile 0's B stage runs while they work on tile 1.
+// TMEM (512 columns): tile g owns columns [256g, 256g + 256): S^T and dP^T in
 // [0, 2H); then, per 16-head chunk k, P^T in [16k, 16k + 8) and scale*dS^T in
-// [16k + 8, 16k + 16) (bf16 pairs over the chunk's own S^T columns), and the
-// interm accumulator in [128, 256).
+// [16k + 8, 16k + 16) (bf16 pairs over chunk k of whichever of S^T / dP^T owns
+// [0, H)), and the interm accumulator in [128, 256).
 //
 // dq_kernel: persistent; item = (token, half of D). dq = (scale*dS) x kv:
 // M = 128 (heads, zero-padded), N = 256, K = ranks in 64-rank steps, both
@@ -40,6 +45,8 @@
 #include "sm100.cuh"
 #include "tmap.h"
 
+#include <type_traits>
+
 namespace smla {
 using namespace sm100;
 
@@ -52,7 +59,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 #ifdef SMLA_TRACE
 // Optional phase timestamps (compiled only with -DSMLA_TRACE; the library
 // build leaves them out): per kernel, CTA (< 8) and item (< 8), 64 events.
-constexpr int kTraceCtas = 8, kTraceItems = 8, kTraceEvents = 64;
+constexpr int kTraceCtas = 8, kTraceItems = 8, kTraceEvents = 128;
 __device__ unsigned long long g_smla_trace[2 * kTraceCtas * kTraceItems * kTraceEvents];
 // per kernel and CTA (< 1024): start and end time of the CTA's MMA thread
 __device__ unsigned long long g_smla_cta_span[2 * 1024 * 3];
@@ -74,9 +81,18 @@ __device__ __forceinline__ unsigned smla_smid() {
             g_smla_trace[(((kid) * kTraceCtas + blockIdx.x) * kTraceItems + (it)) *         \
                              kTraceEvents + (ev)] = globaltimer_ns();                       \
     } while (0)
+#define SMLA_TRACE_VAL(kid, it, ev, val)                                                    \
+    do {                                                                                    \
+        if (blockIdx.x < kTraceCtas && (it) < kTraceItems)                                  \
+            g_smla_trace[(((kid) * kTraceCtas + blockIdx.x) * kTraceItems + (it)) *         \
+                             kTraceEvents + (ev)] = (val);                                  \
+    } while (0)
 #else
 #define SMLA_TRACE_EV(kid, it, ev) \
     do {                           \
+    } while (0)
+#define SMLA_TRACE_VAL(kid, it, ev, val) \
+    do {                                 \
     } while (0)
 #define SMLA_TRACE_SPAN(kid, which) \
     do {                            \
@@ -125,11 +141,17 @@ struct SdiParams {
     const float* lse;
     const float* delta;
     uint16_t* interm;     // [T, R, 512]
+    uint16_t* dsT;        // scale*dS^T stash [T, ds_rows, Hp]
     int T, K, N, r0, R, Rp, Hp;
     int ds_rows, ds_off;  // stash rank rows per token; this chunk's first row
     int npairs;           // items per token: ceil(R / 256)
     int tiles_last;       // tiles (1 or 2) in a token's last item
     float scale;
+    // q / dO loads: 0 = separate [H x 64] boxes of q and dO; 1 = one paired box
+    // per load with q first; 2 = paired, dO first (dO sits below q in memory).
+    // The tensor that comes first in shared memory owns TMEM columns [0, H) of
+    // the S^T | dP^T accumulator and the first half of each B-stage slot.
+    int qd_mode;
     unsigned* status;
 };
 
@@ -141,15 +163,32 @@ struct SdiShared {
     // (a parity wait on `empty`, which advances on every use, could see the
     // slot two phases on and pass too early)
     uint64_t kempty[8];
-    uint64_t s_full, p_ready, x_full[2], x_empty[2], b_done[2], drain;
+    uint64_t s_full[2], p_ready[2], x_full[2], x_empty[2], b_done[2], drain;
     uint32_t tbase;
     volatile int abort_flag;
 };
 
 // Per epilogue warp: a 32-row x 128-byte staging tile that turns one-row-per-
-// lane TMEM data into one TMA store; 16-byte pieces are placed with the
-// 128-byte swizzle the store's tensor map uses (which also spreads banks).
+// lane TMEM data into one TMA store; the 16-byte piece j of row r sits at
+// piece slot j ^ (r & 7), the 128-byte swizzle of the store's tensor map
+// (which also keeps the row-per-lane writes free of bank conflicts). Two
+// alternatives measured slower: plain coalesced stores from the staging tile
+// (they add the L1 data path to the shared-memory traffic the tensor cores
+// need) and 32-byte stores straight from registers, one rank row per lane.
 constexpr int kStageBytes = 32 * 128;
+
+// Writes the warp's staged 32 rows x 128 bytes to global memory with plain
+// coalesced stores (8 lanes per row, four rows per instruction): row r goes to
+// base + r * row_elems (bf16 elements), rows r >= nrows are skipped.
+__device__ __forceinline__ void store_staged_rows(const uint8_t* stage, uint16_t* base, int64_t row_elems,
+                                                  int nrows, int lane) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int rr = 4 * k + (lane >> 3), piece = lane & 7;
+        const uint4 val = reinterpret_cast<const uint4*>(stage + rr * 128)[piece ^ (rr & 7)];
+        if (rr < nrows) reinterpret_cast<uint4*>(base + rr * row_elems)[piece] = val;
+    }
+}
 
 template <int H>
 struct SdiCfg {
@@ -170,6 +209,7 @@ struct SdiCfg {
 template <int H>
 __global__ void __launch_bounds__(384, 1)
 sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+           const __grid_constant__ CUtensorMap map_qda, const __grid_constant__ CUtensorMap map_qdb,
            const __grid_constant__ CUtensorMap map_im, const __grid_constant__ CUtensorMap map_ds,
            const SdiParams p) {
     using C = SdiCfg<H>;
@@ -186,11 +226,11 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             mbar_init(&sh.empty[s], 1);
             mbar_init(&sh.kempty[s], 1);
         }
-        mbar_init(&sh.s_full, 1);
-        mbar_init(&sh.p_ready, 8);
         for (int g = 0; g < 2; ++g) {
+            mbar_init(&sh.s_full[g], 1);   // tile g's S^T | dP^T are complete
+            mbar_init(&sh.p_ready[g], 8);  // all 8 epilogue warps wrote tile g's P / dS
             mbar_init(&sh.x_full[g], 1);   // tile g's interm accumulator is ready
-            mbar_init(&sh.x_empty[g], 4);  // tile g's 4 epilogue warps have read it
+            mbar_init(&sh.x_empty[g], 8);  // all 8 epilogue warps have read their halves
             mbar_init(&sh.b_done[g], 1);
         }
         mbar_init(&sh.drain, 1);
@@ -212,6 +252,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             int it = 0;
             for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
                 SMLA_TRACE_EV(0, it, 0);
+                SMLA_TRACE_VAL(0, it, 45, uint64_t(p.qd_mode));
                 const int t = item / p.npairs;
                 for (int c = 0; c < C::kUses; ++c) {
                     ok = wait_or_abort(&sh.empty[slot], phase ^ 1u, &sh.abort_flag, p.status);
@@ -221,17 +262,25 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     if (c < 8) {
                         // A stage: q and dO columns [64c, 64c + 64)
                         mbar_arrive_expect_tx(&sh.full[slot], 2 * C::kQBytes);
-                        tma_load_2d(sb, &map_q, c * 64, t * H, &sh.full[slot]);
-                        tma_load_2d(sb + C::kQBytes, &map_do, c * 64, t * H, &sh.full[slot]);
+                        if (p.qd_mode != 0) {
+                            tma_load_5d(sb, &map_qda, 0, 0, c, 0, t, &sh.full[slot]);
+                        } else {
+                            tma_load_2d(sb, &map_q, c * 64, t * H, &sh.full[slot]);
+                            tma_load_2d(sb + C::kQBytes, &map_do, c * 64, t * H, &sh.full[slot]);
+                        }
                     } else {
                         // B stage: q and dO columns [128b, 128b + 128), two 64-column
                         // blocks each; the copy warps skip these uses, so arrive for them.
                         const int b = c - 8;
                         mbar_arrive_expect_tx(&sh.full[slot], 4 * C::kQBytes);
-                        tma_load_2d(sb, &map_q, b * 128, t * H, &sh.full[slot]);
-                        tma_load_2d(sb + C::kQBytes, &map_q, b * 128 + 64, t * H, &sh.full[slot]);
-                        tma_load_2d(sb + 2 * C::kQBytes, &map_do, b * 128, t * H, &sh.full[slot]);
-                        tma_load_2d(sb + 3 * C::kQBytes, &map_do, b * 128 + 64, t * H, &sh.full[slot]);
+                        if (p.qd_mode != 0) {
+                            tma_load_5d(sb, &map_qdb, 0, 0, 2 * b, 0, t, &sh.full[slot]);
+                        } else {
+                            tma_load_2d(sb, &map_q, b * 128, t * H, &sh.full[slot]);
+                            tma_load_2d(sb + C::kQBytes, &map_q, b * 128 + 64, t * H, &sh.full[slot]);
+                            tma_load_2d(sb + 2 * C::kQBytes, &map_do, b * 128, t * H, &sh.full[slot]);
+                            tma_load_2d(sb + 3 * C::kQBytes, &map_do, b * 128 + 64, t * H, &sh.full[slot]);
+                        }
                         mbar_arrive_cnt(&sh.full[slot], 64);
                     }
                     ++issued;
@@ -335,6 +384,10 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             int slot = 0; uint32_t phase = 0;
             uint32_t xe_done[2] = {0, 0};   // drains of tile g's accumulator seen
             uint32_t x_uses[2] = {0, 0};    // accumulations of tile g issued
+            uint32_t p_seen[2] = {0, 0};    // phases of p_ready[g] waited for
+            // B-stage slot offsets of the dO blocks (P term) and q blocks (dS term)
+            const uint32_t do_off = p.qd_mode == 2 ? 0u : 2u * C::kQBytes;
+            const uint32_t q_off = p.qd_mode == 2 ? 2u * C::kQBytes : 0u;
             bool ok = true;
             int it = 0;
             for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
@@ -345,6 +398,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 if (it > 0) {
                     ok = ok && wait_or_abort(&sh.b_done[0], (it - 1) & 1, &sh.abort_flag, p.status);
                     ok = ok && wait_or_abort(&sh.b_done[1], (it - 1) & 1, &sh.abort_flag, p.status);
+                    SMLA_TRACE_EV(0, it, 1);
                     // ... and after its drains, which follow the dS stash (the stash
                     // reads P^T / dS^T columns that this A stage overwrites)
                     for (int g = 0; g < 2 && ok; ++g)
@@ -352,6 +406,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                             ok = wait_or_abort(&sh.x_empty[g], xe_done[g] & 1u, &sh.abort_flag, p.status);
                             ++xe_done[g];
                         }
+                    SMLA_TRACE_EV(0, it, 2);
                 }
                 SMLA_TRACE_EV(0, it, 3);
                 for (int c = 0; c < 8 && ok; ++c) {
@@ -365,19 +420,19 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                         for (int k = 0; k < 4; ++k)
                             mma_ss(tbase + g * 256, sdesc_sw128(kvb + k * 32, 16, 1024),
                                    sdesc_sw128(sb + k * 32, 16, 1024), C::kIdescA, (c | k) != 0);
+                        // tile 0's S^T | dP^T are complete one tile-step before tile 1's:
+                        // its epilogue starts while tile 1's last MMAs run
+                        if (c == 7) mma_commit(&sh.s_full[g]);
                     }
                     mma_commit(&sh.empty[slot]);
                     if ((c + C::kSlots) % C::kUses < 8) mma_commit(&sh.kempty[slot]);
                     advance(slot, phase, C::kSlots);
                 }
                 if (!ok) break;
-                mma_commit(&sh.s_full);
                 SMLA_TRACE_EV(0, it, 4);
-                ok = wait_or_abort(&sh.p_ready, it & 1, &sh.abort_flag, p.status);
-                if (!ok) break;
-                SMLA_TRACE_EV(0, it, 5);
-                tc_fence_after();
-                // B stage: interm columns [128c, 128c + 128), tiles alternating.
+                // B stage: interm columns [128c, 128c + 128), tiles alternating; tile
+                // g's first step waits for its P / dS, so tile 0's B stage runs while
+                // the epilogue warps work on tile 1.
                 for (int c = 0; c < 4 && ok; ++c) {
                     ok = wait_or_abort(&sh.full[slot], phase, &sh.abort_flag, p.status);
                     SMLA_TRACE_EV(0, it, 16 + c);
@@ -385,6 +440,12 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     tc_fence_after();
                     const uint32_t sb = smem_u32(slots + slot * C::kSlotBytes);
                     for (int g = 0; g < ntiles && ok; ++g) {
+                        if (c == 0) {
+                            ok = wait_or_abort(&sh.p_ready[g], p_seen[g] & 1u, &sh.abort_flag, p.status);
+                            ++p_seen[g];
+                            if (!ok) break;
+                            if (g == 0) SMLA_TRACE_EV(0, it, 5);
+                        }
                         while (ok && xe_done[g] < x_uses[g]) {
                             ok = wait_or_abort(&sh.x_empty[g], xe_done[g] & 1u, &sh.abort_flag, p.status);
                             ++xe_done[g];
@@ -399,7 +460,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                             const int kk = pterm ? ks : ks - H / 16;
                             const uint32_t acol = kk * 16 + (pterm ? 0 : 8);
                             // dO (P term) or q (dS term): two 64-column blocks of H rows
-                            const uint32_t bt = (pterm ? sb + 2 * C::kQBytes : sb) + kk * 2048;
+                            const uint32_t bt = sb + (pterm ? do_off : q_off) + kk * 2048;
                             mma_ts(tile + 128, tile + acol, sdesc_sw128(bt, C::kQBytes, 1024),
                                    C::kIdescB, ks != 0);
                         }
@@ -423,40 +484,45 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         __syncwarp();
     } else {
         // ----------------------------------------------------------- epilogue
-        const int g = (warp - 2) >> 2;                  // tile of this warp group
+        // All eight warps work on every tile. Warp w reads TMEM lane quarter w & 3
+        // (ranks 32 (w & 3) .. + 31 of a tile); its group G = (w - 2) >> 2 takes
+        // one half of each job: head chunks [0, kSplit) or [kSplit, H / 16) of the
+        // P / dS pass, 64-head block G of the dS^T stash, and interm columns
+        // [64G, 64G + 64) of each drain. Tile 0 is finished first, so that its B
+        // stage starts while the warps work on tile 1.
+        const int grp = (warp - 2) >> 2;
         const int quarter = warp & 3;                   // TMEM lane quarter of this warp
-        const int r = quarter * 32 + lane;              // TMEM lane = rank inside the tile
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
         uint8_t* stage = slots + C::kSlots * C::kSlotBytes + (warp - 2) * kStageBytes;
-        float* lsd = reinterpret_cast<float*>(stage);   // [0, H): lse*log2(e); [H, 2H): delta
+        float* lsd = reinterpret_cast<float*>(stage);   // [0, H): -lse*log2(e); [H, 2H): -scale*delta
         static_assert(2 * H * 4 <= kStageBytes, "lse / delta must fit the staging tile");
+        constexpr int kChunks = H / 16;                 // 16-head chunks
+        constexpr int kSplit = (kChunks + 1) / 2;       // group 0's chunks: [0, kSplit)
         const float c1 = p.scale * kLog2e;
+        const float2 c1v = make_float2(c1, c1), scv = make_float2(p.scale, p.scale);
+        // TMEM columns of S^T and dP^T (whichever of q / dO came first owns [0, H))
+        const uint32_t s_col = p.qd_mode == 2 ? uint32_t(H) : 0u;
+        const uint32_t dp_col = p.qd_mode == 2 ? 0u : uint32_t(H);
         constexpr int kHw = (H + 31) / 32;              // head words per lane
-        uint32_t x_use = 0;                             // accumulations of this tile consumed
+        uint32_t s_seen0 = 0, s_seen1 = 0;              // phases of s_full[0 / 1] consumed
+        uint32_t p_arr0 = 0, p_arr1 = 0;                // phases of p_ready[0 / 1] arrived on
+        uint32_t x_use0 = 0, x_use1 = 0;                // accumulations of tile 0 / 1 consumed
         int it = 0;
         for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++it) {
             if (__any_sync(0xffffffffu, sh.abort_flag != 0)) break;
             const int t = item / p.npairs, pr = item - t * p.npairs;
             const int ntiles = pr == p.npairs - 1 ? p.tiles_last : 2;
-            const bool active = g < ntiles;
-            const int rl = pr * 256 + g * 128 + r;
-            const int row0 = pr * 256 + g * 128 + quarter * 32;   // first rank of this warp
-            // lane l holds lse * log2(e) and delta of heads l, l + 32, ...
+            // lane l holds -lse * log2(e) and -scale * delta of heads l, l + 32, ...
             float lse_w[kHw], del_w[kHw];
 #pragma unroll
             for (int k = 0; k < kHw; ++k) {
                 const int h = k * 32 + lane;
-                lse_w[k] = h < H ? __ldg(p.lse + int64_t(t) * H + h) * kLog2e : 0.f;
-                del_w[k] = h < H ? __ldg(p.delta + int64_t(t) * H + h) : 0.f;
+                lse_w[k] = h < H ? -(__ldg(p.lse + int64_t(t) * H + h) * kLog2e) : 0.f;
+                del_w[k] = h < H ? -(p.scale * __ldg(p.delta + int64_t(t) * H + h)) : 0.f;
             }
-            bool valid = false;
-            if (active && rl < p.R) {
-                const int j = __ldg(p.topk + int64_t(t) * p.K + p.r0 + rl);
-                valid = j >= 0 && j < p.N;
-            }
-            // lse * log2(e) and delta of every head go to the head of this warp's
-            // staging tile (free once its last TMA store has read it), from where
-            // each lane reads them as shared-memory broadcasts
+            // -lse * log2(e) and -scale * delta of every head go to the head of this
+            // warp's staging tile (free once its last TMA store has read it), from
+            // where each lane reads them as shared-memory broadcasts
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
 #pragma unroll
@@ -465,130 +531,163 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 if (h < H) { lsd[h] = lse_w[k]; lsd[H + h] = del_w[k]; }
             }
             __syncwarp();
-            if (!wait_or_abort_warp(&sh.s_full, it & 1, &sh.abort_flag, p.status)) break;
-            if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 7);
-            if (warp == 9 && lane == 0) SMLA_TRACE_EV(0, it, 44);
-            __syncwarp();
-            tc_fence_after();
-            if (active) {
-                const uint32_t trow = tbase + lane_off + g * 256;
-#pragma unroll
-                for (int c16 = 0; c16 < H / 16; c16 += 2) {
-                    const int nch = (c16 + 1 < H / 16) ? 2 : 1;
-                    uint32_t sv[2][16], dv[2][16];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u)
-                        if (u < nch) {
-                            tmem_ld16(trow + (c16 + u) * 16, sv[u]);
-                            tmem_ld16(trow + H + (c16 + u) * 16, dv[u]);
-                        }
-                    tmem_wait_ld();
-                    if (c16 == 0 && warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 10);
-                    if (c16 == 0 && warp == 9 && lane == 0) SMLA_TRACE_EV(0, it, 60);
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        if (u >= nch) break;
-                        const int k = c16 + u;              // head chunk: heads 16k .. 16k + 15
-                        float l2v[16], dev[16];
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const float4 a = reinterpret_cast<const float4*>(lsd + k * 16)[v];
-                            const float4 b = reinterpret_cast<const float4*>(lsd + H + k * 16)[v];
-                            l2v[4 * v] = a.x; l2v[4 * v + 1] = a.y; l2v[4 * v + 2] = a.z; l2v[4 * v + 3] = a.w;
-                            dev[4 * v] = b.x; dev[4 * v + 1] = b.y; dev[4 * v + 2] = b.z; dev[4 * v + 3] = b.w;
-                        }
-                        uint32_t pp[8], dd[8];
-#pragma unroll
-                        for (int j2 = 0; j2 < 8; ++j2) {
-                            float pv[2], dsv[2];
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const float s = __uint_as_float(sv[u][2 * j2 + e]);
-                                const float dp = __uint_as_float(dv[u][2 * j2 + e]);
-                                const float pe = valid ? ex2_approx(fmaf(s, c1, -l2v[2 * j2 + e])) : 0.f;
-                                pv[e] = pe;
-                                dsv[e] = valid ? p.scale * pe * (dp - dev[2 * j2 + e]) : 0.f;
-                            }
-                            pp[j2] = pack_bf16x2(pv[0], pv[1]);
-                            dd[j2] = pack_bf16x2(dsv[0], dsv[1]);
-                        }
-                        // P^T and scale*dS^T of chunk k over its S^T columns, already read
-                        tmem_st8(trow + k * 16, pp);
-                        tmem_st8(trow + k * 16 + 8, dd);
-                    }
-                }
-                if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 11);
-                if (warp == 9 && lane == 0) SMLA_TRACE_EV(0, it, 61);
-                tmem_wait_st();
-                if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 12);
-                if (warp == 9 && lane == 0) SMLA_TRACE_EV(0, it, 62);
-            }
-            if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 13);
-            if (warp == 9 && lane == 0) SMLA_TRACE_EV(0, it, 63);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.p_ready);
-            if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 8);
-            if (active) {
-                // P^T and dS^T are read by the B-stage MMAs from here on (read only);
-                // the stash reads dS^T alongside them. The next item's A stage
-                // overwrites these columns only after this warp's drains below.
-                __syncwarp();               // tcgen05.ld is warp-collective
-                const uint32_t trow = tbase + lane_off + g * 256;
-                // stash scale * dS^T for the dq kernel: per 64-head block the warp's 32
-                // rows are read back from TMEM, go through the staging tile and leave
-                // in one TMA store (heads >= H are 0)
-#pragma unroll
-                for (int hb = 0; hb < (H + 63) / 64; ++hb) {
-                    uint32_t dsw[32];
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const int k = hb * 4 + q4;
-                        if (k < H / 16) tmem_ld8(trow + k * 16 + 8, dsw + 8 * q4);
-                    }
-                    tmem_wait_ld();
-                    if (lane == 0) bulk_wait_read_all();
-                    __syncwarp();
-                    uint4* srow = reinterpret_cast<uint4*>(stage + lane * 128);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const int k = hb * 4 + (v >> 1);
-                        srow[v ^ (lane & 7)] = k < H / 16
-                            ? make_uint4(dsw[4 * v], dsw[4 * v + 1], dsw[4 * v + 2], dsw[4 * v + 3])
-                            : make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&map_ds, hb * 64, t * p.ds_rows + p.ds_off + row0, stage);
-                        bulk_commit();
-                    }
-                    __syncwarp();
-                }
-            }
-            // drain interm columns [128c, 128c + 128) of this warp's tile, in halves
             bool ok = true;
-            for (int c = 0; c < 4 && active; ++c) {
-                if (!wait_or_abort_warp(&sh.x_full[g], x_use & 1u, &sh.abort_flag, p.status)) {
-                    ok = false;
-                    break;
+            // ---- P and scale*dS of each tile, written back into TMEM as bf16 pairs
+            for (int g2 = 0; g2 < ntiles && ok; ++g2) {
+                const int rl = pr * 256 + g2 * 128 + quarter * 32 + lane;   // this lane's rank
+                bool valid = false;
+                if (rl < p.R) {
+                    const int j = __ldg(p.topk + int64_t(t) * p.K + p.r0 + rl);
+                    valid = j >= 0 && j < p.N;
                 }
-                ++x_use;
-                if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 32 + c);
+                const uint32_t sphase = (g2 ? s_seen1 : s_seen0) & 1u;
+                if (g2) ++s_seen1; else ++s_seen0;
+                if (!wait_or_abort_warp(&sh.s_full[g2], sphase, &sh.abort_flag, p.status)) { ok = false; break; }
+                if (lane == 0 && warp == 2) SMLA_TRACE_EV(0, it, g2 ? 46 : 7);
+                if (lane == 0 && warp == 9 && g2 == 0) SMLA_TRACE_EV(0, it, 44);
                 __syncwarp();
                 tc_fence_after();
-                for (int hh = 0; hh < 2; ++hh) {
-                    __syncwarp();           // lane 0 may still be in the previous half's store
-                    const uint32_t xa = tbase + lane_off + g * 256 + 128 + 64 * hh;
+                const uint32_t trow = tbase + lane_off + g2 * 256;
+                // P = 2^(S * scale * log2(e) - lse * log2(e)) and
+                // scale*dS = P * (scale * dP - scale * delta), two heads per packed
+                // fp32x2 operation, over head chunks [K0, K1). Ranks that are masked
+                // or past the chunk's end get P = dS = 0 (their bf16 words are
+                // cleared); a warp whose 32 ranks are all valid skips that step.
+                const uint32_t vmask = valid ? 0xffffffffu : 0u;
+                auto pds = [&](auto k0_tag, auto k1_tag, auto masked_tag) {
+                    constexpr int K0 = decltype(k0_tag)::value, K1 = decltype(k1_tag)::value;
+                    constexpr bool kMasked = decltype(masked_tag)::value;
+#pragma unroll
+                    for (int c16 = K0; c16 < K1; c16 += 2) {
+                        const int nch = (c16 + 1 < K1) ? 2 : 1;
+                        uint32_t sv[2][16], dv[2][16];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+                            if (u < nch) {
+                                tmem_ld16(trow + s_col + (c16 + u) * 16, sv[u]);
+                                tmem_ld16(trow + dp_col + (c16 + u) * 16, dv[u]);
+                            }
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            if (u >= nch) break;
+                            const int k = c16 + u;              // head chunk: heads 16k .. 16k + 15
+                            float2 nl[8], nd[8];
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                const float4 a = reinterpret_cast<const float4*>(lsd + k * 16)[v];
+                                const float4 b = reinterpret_cast<const float4*>(lsd + H + k * 16)[v];
+                                nl[2 * v] = make_float2(a.x, a.y); nl[2 * v + 1] = make_float2(a.z, a.w);
+                                nd[2 * v] = make_float2(b.x, b.y); nd[2 * v + 1] = make_float2(b.z, b.w);
+                            }
+                            uint32_t pp[8], dd[8];
+#pragma unroll
+                            for (int j2 = 0; j2 < 8; ++j2) {
+                                const float2 sp2 = make_float2(__uint_as_float(sv[u][2 * j2]),
+                                                               __uint_as_float(sv[u][2 * j2 + 1]));
+                                const float2 dp2 = make_float2(__uint_as_float(dv[u][2 * j2]),
+                                                               __uint_as_float(dv[u][2 * j2 + 1]));
+                                const float2 arg = __ffma2_rn(sp2, c1v, nl[j2]);
+                                const float2 pe = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
+                                const float2 ds = __fmul2_rn(pe, __ffma2_rn(dp2, scv, nd[j2]));
+                                pp[j2] = pack_bf16x2(pe.x, pe.y);
+                                dd[j2] = pack_bf16x2(ds.x, ds.y);
+                                if constexpr (kMasked) { pp[j2] &= vmask; dd[j2] &= vmask; }
+                            }
+                            // P^T and scale*dS^T of chunk k over its columns [16k, 16k + 16)
+                            // (chunk k of S^T or of dP^T), already read above
+                            tmem_st8(trow + k * 16, pp);
+                            tmem_st8(trow + k * 16 + 8, dd);
+                        }
+                    }
+                };
+                using Z = std::integral_constant<int, 0>;
+                using S = std::integral_constant<int, kSplit>;
+                using E = std::integral_constant<int, kChunks>;
+                const bool all_valid = __all_sync(0xffffffffu, valid);
+                if (grp == 0) {
+                    if (all_valid) pds(Z{}, S{}, std::false_type{});
+                    else pds(Z{}, S{}, std::true_type{});
+                } else {
+                    if (all_valid) pds(S{}, E{}, std::false_type{});
+                    else pds(S{}, E{}, std::true_type{});
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.p_ready[g2]);
+                if (g2) ++p_arr1; else ++p_arr0;
+                if (lane == 0 && warp == 2) SMLA_TRACE_EV(0, it, g2 ? 47 : 8);
+            }
+            if (!ok) break;
+            // ---- stash scale * dS^T for the dq kernel: 64-head block `grp` of the
+            // warp's 32 rows of tile g2, read back from TMEM (the B-stage MMAs read
+            // the same columns; the next item's A stage overwrites them only after
+            // this warp's last drain), staged and stored by TMA. Heads >= H are 0;
+            // rows past the chunk's end carry dS = 0. A 64-head block may hold
+            // chunks the other group wrote, so it is read only once all eight
+            // warps have arrived on the tile's p_ready. It runs after the tile's
+            // first drain, under the next MMAs rather than before the drains.
+            auto stash = [&](int g2) -> bool {
+                if (grp * 64 >= H) return true;
+                const uint32_t pphase = ((g2 ? p_arr1 : p_arr0) - 1u) & 1u;
+                if (!wait_or_abort_warp(&sh.p_ready[g2], pphase, &sh.abort_flag, p.status)) return false;
+                tc_fence_after();
+                const int row0 = pr * 256 + g2 * 128 + quarter * 32;   // first rank of these rows
+                const uint32_t trow = tbase + lane_off + g2 * 256;
+                uint32_t dsw[32];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int k = grp * 4 + q4;
+                    if (k < kChunks) tmem_ld8(trow + k * 16 + 8, dsw + 8 * q4);
+                }
+                tmem_wait_ld();
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+                uint4* srow = reinterpret_cast<uint4*>(stage + lane * 128);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const int k = grp * 4 + (v >> 1);
+                    srow[v ^ (lane & 7)] = k < kChunks
+                        ? make_uint4(dsw[4 * v], dsw[4 * v + 1], dsw[4 * v + 2], dsw[4 * v + 3])
+                        : make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&map_ds, grp * 64, t * p.ds_rows + p.ds_off + row0, stage);
+                    bulk_commit();
+                }
+                __syncwarp();
+                return true;
+            };
+            // ---- drain interm columns [128c, 128c + 128) of every tile, tiles
+            // alternating as the MMA issues them; this warp takes columns
+            // [64 grp, 64 grp + 64) of its lane quarter
+            for (int c = 0; c < 4 && ok; ++c) {
+                for (int g2 = 0; g2 < ntiles; ++g2) {
+                    const uint32_t xu = g2 ? x_use1 : x_use0;
+                    if (!wait_or_abort_warp(&sh.x_full[g2], xu & 1u, &sh.abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (g2) ++x_use1; else ++x_use0;
+                    if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 32 + 2 * c + g2);
+                    if (lane == 0 && (warp == 2 || warp == 9))
+                        SMLA_TRACE_EV(0, it, (warp == 2 ? 64 : 96) + 3 * (2 * c + g2));
+                    __syncwarp();
+                    tc_fence_after();
+                    const uint32_t xa = tbase + lane_off + g2 * 256 + 128 + 64 * grp;
                     uint32_t v0[32], v1[32];
                     tmem_ld32(xa, v0);
                     tmem_ld32(xa + 32, v1);
                     tmem_wait_ld();
-                    if (hh == 1) {   // the accumulator is read: the MMA may reuse it
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&sh.x_empty[g]);
-                    }
+                    // the accumulator is read: the MMA may reuse it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.x_empty[g2]);
+                    if (lane == 0 && (warp == 2 || warp == 9))
+                        SMLA_TRACE_EV(0, it, (warp == 2 ? 64 : 96) + 3 * (2 * c + g2) + 1);
                     if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
                     uint4* srow = reinterpret_cast<uint4*>(stage + lane * 128);
@@ -596,27 +695,27 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     for (int v = 0; v < 4; ++v) srow[v ^ (lane & 7)] = pack8(v0 + 8 * v);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) srow[(v + 4) ^ (lane & 7)] = pack8(v1 + 8 * v);
-                    const int col = 128 * c + 64 * hh;
-                    if (row0 + 32 <= p.R) {
-                        // the warp's 32 ranks all belong to this token: one TMA store
+                    const int col = 128 * c + 64 * grp;
+                    const int drow0 = pr * 256 + g2 * 128 + quarter * 32;   // first rank of these rows
+                    if (drow0 + 32 <= p.R) {
+                        // the warp's 32 ranks all belong to this chunk: one TMA store
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(&map_im, col, t * p.R + row0, stage);
+                            tma_store_2d(&map_im, col, t * p.R + drow0, stage);
                             bulk_commit();
                         }
                     } else {
-                        // ragged last rows of a token: plain stores of the rows < R
+                        // ragged last rows: plain stores of the rows < R
                         __syncwarp();
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const int rr = 4 * k + (lane >> 3), piece = lane & 7;
-                            const uint4 val = reinterpret_cast<const uint4*>(stage + rr * 128)[piece ^ (rr & 7)];
-                            if (row0 + rr < p.R)
-                                reinterpret_cast<uint4*>(p.interm + (int64_t(t) * p.R + row0 + rr) * kD + col)[piece] = val;
-                        }
-                        __syncwarp();
+                        store_staged_rows(stage, p.interm + (int64_t(t) * p.R + drow0) * kD + col, kD,
+                                          p.R - drow0, lane);
                     }
+                    __syncwarp();
+                    if (lane == 0 && (warp == 2 || warp == 9))
+                        SMLA_TRACE_EV(0, it, (warp == 2 ? 64 : 96) + 3 * (2 * c + g2) + 2);
+                    if (c == 0 && !stash(g2)) { ok = false; break; }
+                    if (c == 0 && g2 == ntiles - 1 && lane == 0 && warp == 2) SMLA_TRACE_EV(0, it, 14);
                 }
                 if (warp == 2 && lane == 0) SMLA_TRACE_EV(0, it, 40 + c);
             }
@@ -944,7 +1043,21 @@ cudaError_t launch_sdi_h(const ChunkArgs& a, cudaStream_t s) {
     if (set_smem_attrs_once(reinterpret_cast<const void*>(sdi_kernel<H>), C::kSmem, attr_done))
         return cudaErrorInvalidValue;
     const int Rp = round_up_ranks(a.R), Hp = pad_heads(H);
-    CUtensorMap mq, mdo, mim, mds;
+    CUtensorMap mq, mdo, mqda, mqdb, mim, mds;
+    // q and dO as one paired tensor (one TMA box per ring slot instead of two or
+    // four) when their distance is a stride the tensor map can encode
+    int qd_mode = 0;
+    {
+        const uintptr_t uq = reinterpret_cast<uintptr_t>(a.q), ud = reinterpret_cast<uintptr_t>(a.dO);
+        const bool q_first = uq < ud;
+        const void* lo = q_first ? static_cast<const void*>(a.q) : static_cast<const void*>(a.dO);
+        const uint64_t dist = q_first ? uint64_t(ud - uq) : uint64_t(uq - ud);
+        if (make_tmap_bf16_pair5d(&mqda, lo, dist, uint64_t(a.T), H, 1) &&
+            make_tmap_bf16_pair5d(&mqdb, lo, dist, uint64_t(a.T), H, 2))
+            qd_mode = q_first ? 1 : 2;
+        else
+            mqda = mqdb = CUtensorMap{};
+    }
     if (!make_tmap_bf16_2d(&mq, a.q, uint64_t(a.T) * H, kD, kD, H, 64, true) ||
         !make_tmap_bf16_2d(&mdo, a.dO, uint64_t(a.T) * H, kD, kD, H, 64, true) ||
         !make_tmap_bf16_2d(&mim, a.interm, uint64_t(a.T) * a.R, kD, kD, 32, 64, true) ||
@@ -953,14 +1066,16 @@ cudaError_t launch_sdi_h(const ChunkArgs& a, cudaStream_t s) {
     SdiParams sp{};
     sp.ds_rows = a.ds_rows; sp.ds_off = a.ds_off;
     sp.kv = a.kv; sp.topk = a.topk; sp.lse = a.lse; sp.delta = a.delta; sp.interm = a.interm;
+    sp.dsT = a.dsT;
     sp.T = a.T; sp.K = a.K; sp.N = a.N; sp.r0 = a.r0; sp.R = a.R; sp.Rp = Rp; sp.Hp = Hp;
     sp.npairs = (a.R + 255) / 256;
     sp.tiles_last = (a.R - (sp.npairs - 1) * 256) > 128 ? 2 : 1;
     sp.scale = a.scale; sp.status = a.status;
+    sp.qd_mode = qd_mode;
     const int64_t items = int64_t(a.T) * sp.npairs;
     const int sms = sm_count();
     const int grid = int(items < sms ? items : sms);
-    sdi_kernel<H><<<grid, C::kThreads, C::kSmem, s>>>(mq, mdo, mim, mds, sp);
+    sdi_kernel<H><<<grid, C::kThreads, C::kSmem, s>>>(mq, mdo, mqda, mqdb, mim, mds, sp);
     note_launch();
     return cudaGetLastError();
 }

@@ -83,6 +83,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int
 }
 
 // Prefetch one box of a 2-D tiled tensor into L2 (no shared-memory destination).
+// 5-D tiled load of one box into smem at coordinates (c0 .. c4), completing
+// on the mbarrier's transaction count.
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* m, int c0, int c1, int c2,
+                                            int c3, int c4, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                      reinterpret_cast<uint64_t>(m)),

@@ -111,7 +111,10 @@ class Case:
         The GPU forms dP (tensor-core accumulation) and delta (CUDA cores) as
         fp32 sums of the same 512 products dO[t,h,d] * kv[j,d] (exact in fp32)
         in different orders; each sum is within gamma_511 * sum_d |dO * kv| of
-        the exact value (gamma_n = n u / (1 - n u), u = FP32_U). Then
+        the exact value (gamma_n = n u / (1 - n u), u = FP32_U). The kernel
+        forms scale * dS = P * fma(dP, scale, -fl(scale * delta)): rounding
+        scale * delta and the fma result adds at most 2 u * scale * |delta|
+        <= 2 u * scale * sum_d |dO * kv| (|delta| = |sum_d dO * kv| here). Then
         scale * dS is rounded to bf16 (factor 1 + 2^-8), multiplied by kv[j, d]
         and the product rounded to bf16 again (1 + 2^-8); P itself is within
         1e-3 of 1 (P = exp(s - lse) with lse the fp32 rounding of s).
@@ -126,7 +129,7 @@ class Case:
         ok = idx >= 0
         kvr = self.kv64[np.where(ok, idx, 0)]                         # [T, D]
         s_abs = np.abs(self.do64 * kvr[:, None, :]).sum(axis=2)      # [T, H]
-        diff = 2 * gamma * s_abs                                     # |dP - delta| on the GPU
+        diff = (2 * gamma + 2 * FP32_U) * s_abs                      # |dP - delta| on the GPU
         f = 1.001 * (1 + 2.0 ** -8) ** 2 * self.scale
         bound[ok] = (f * diff[:, :, None] * np.abs(kvr)[:, None, :])[ok]
         return bound
