@@ -45,6 +45,7 @@
 #include "sm100.cuh"
 #include "tmap.h"
 
+#include <climits>
 #include <type_traits>
 
 namespace smla {
@@ -152,6 +153,7 @@ struct SdiParams {
     // The tensor that comes first in shared memory owns TMEM columns [0, H) of
     // the S^T | dP^T accumulator and the first half of each B-stage slot.
     int qd_mode;
+    int* work_ctr;        // next work item (zeroed before the launch)
     unsigned* status;
 };
 
@@ -164,9 +166,43 @@ struct SdiShared {
     // slot two phases on and pass too early)
     uint64_t kempty[8];
     uint64_t s_full[2], p_ready[2], x_full[2], x_empty[2], b_done[2], drain;
+    // Work queue: the TMA thread takes items from the global counter and
+    // publishes them in order; every other role reads entry k for its k-th
+    // item (the copy warps one item ahead). An entry >= the item count ends
+    // the CTA's work. CTAs that start late (their SM still busy with another
+    // kernel) simply take fewer items.
+    int item_q[4];
+    uint64_t q_full[4], q_empty[4];
     uint32_t tbase;
     volatile int abort_flag;
 };
+
+constexpr int kQueueReaders = 11;   // 2 copy warps + the MMA thread + 8 epilogue warps
+
+// Entry k of the work queue, read by a whole warp (lane 0 signals the read).
+__device__ __forceinline__ int queue_read_warp(SdiShared& sh, int k, unsigned* status, bool& ok) {
+    const int e = k & 3;
+    if (!wait_or_abort_warp(&sh.q_full[e], uint32_t(k >> 2) & 1u, &sh.abort_flag, status)) {
+        ok = false;
+        return INT_MAX;
+    }
+    const int item = *reinterpret_cast<volatile int*>(&sh.item_q[e]);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.q_empty[e]);
+    return item;
+}
+
+// Entry k of the work queue, read by one thread.
+__device__ __forceinline__ int queue_read_thread(SdiShared& sh, int k, unsigned* status, bool& ok) {
+    const int e = k & 3;
+    if (!wait_or_abort(&sh.q_full[e], uint32_t(k >> 2) & 1u, &sh.abort_flag, status)) {
+        ok = false;
+        return INT_MAX;
+    }
+    const int item = *reinterpret_cast<volatile int*>(&sh.item_q[e]);
+    mbar_arrive(&sh.q_empty[e]);
+    return item;
+}
 
 // Per epilogue warp: a 32-row x 128-byte staging tile that turns one-row-per-
 // lane TMEM data into one TMA store; the 16-byte piece j of row r sits at
@@ -234,6 +270,10 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             mbar_init(&sh.b_done[g], 1);
         }
         mbar_init(&sh.drain, 1);
+        for (int e = 0; e < 4; ++e) {
+            mbar_init(&sh.q_full[e], 1);
+            mbar_init(&sh.q_empty[e], kQueueReaders);
+        }
         sh.abort_flag = 0;
         fence_mbar_init();
     }
@@ -249,8 +289,27 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             int slot = 0; uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            int it = 0;
-            for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
+            int pub = 0, last = -1;       // entries published; the last item published
+            auto publish = [&]() -> bool {
+                const int e = pub & 3;
+                if (pub >= 4 &&
+                    !wait_or_abort(&sh.q_empty[e], uint32_t((pub >> 2) - 1) & 1u, &sh.abort_flag, p.status))
+                    return false;
+                int item = atomicAdd(p.work_ctr, 1);
+                if (item > nitems) item = nitems;
+                sh.item_q[e] = item;
+                mbar_arrive(&sh.q_full[e]);
+                last = item;
+                ++pub;
+                return true;
+            };
+            ok = publish();
+            if (ok && last < nitems) ok = publish();
+            for (int it = 0; ok; ++it) {
+                const int item = sh.item_q[it & 3];
+                if (item >= nitems) break;
+                // entry it + 2 (the copy warps read entry it + 1 during this item)
+                if (last < nitems && !publish()) { ok = false; break; }
                 SMLA_TRACE_EV(0, it, 0);
                 SMLA_TRACE_VAL(0, it, 45, uint64_t(p.qd_mode));
                 const int t = item / p.npairs;
@@ -321,7 +380,8 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 out[i] = j;
             }
         };
-        if (int(blockIdx.x) < nitems) load_idx(blockIdx.x, idx_cur);
+        int cur = queue_read_warp(sh, 0, p.status, ok);
+        if (cur < nitems) load_idx(cur, idx_cur);
 #pragma unroll
         for (int i = 0; i < 32; ++i) idx_nxt[i] = 0;
         const char* kvbase = reinterpret_cast<const char*>(p.kv) + (lane & 7) * 16;
@@ -338,9 +398,10 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         };
         int use = 0;              // this CTA's ring use index
         uint32_t kph = 0;         // per slot: parity of its next kempty phase
-        for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
-            const int pr = item % p.npairs;
+        for (int k = 0; ok && cur < nitems; ++k) {
+            const int pr = cur % p.npairs;
             const int ntiles = pr == p.npairs - 1 ? p.tiles_last : 2;
+            int nxt = nitems;
             for (int c = 0; c < 8; ++c, ++use) {
                 if (use >= C::kSlots) {   // the slot's previous use must be consumed
                     if (lane == 0)
@@ -366,15 +427,16 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     // signal what is left, then load the next item's indices
                     cp_async_wait<0>();
                     while (npend > 0) flush_one();
-                    const int next = item + gridDim.x;
-                    if (next < nitems) load_idx(next, idx_nxt);
+                    nxt = queue_read_warp(sh, k + 1, p.status, ok);
+                    if (nxt < nitems) load_idx(nxt, idx_nxt);
                 }
                 advance(slot, phase, C::kSlots);
             }
             // the B-stage uses of the ring are signalled by the TMA thread
-            for (int k = 8; k < C::kUses; ++k, ++use) advance(slot, phase, C::kSlots);
+            for (int u = 8; u < C::kUses; ++u, ++use) advance(slot, phase, C::kSlots);
 #pragma unroll
             for (int i = 0; i < 32; ++i) idx_cur[i] = idx_nxt[i];
+            cur = nxt;
         }
         cp_async_wait<0>();
     } else if (warp == 1) {
@@ -389,8 +451,9 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             const uint32_t do_off = p.qd_mode == 2 ? 0u : 2u * C::kQBytes;
             const uint32_t q_off = p.qd_mode == 2 ? 2u * C::kQBytes : 0u;
             bool ok = true;
-            int it = 0;
-            for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
+            for (int it = 0; ok; ++it) {
+                const int item = queue_read_thread(sh, it, p.status, ok);
+                if (!ok || item >= nitems) break;
                 const int pr = item % p.npairs;
                 const int ntiles = pr == p.npairs - 1 ? p.tiles_last : 2;
                 // A stage may overwrite TMEM only after the previous item's B stage
@@ -507,9 +570,11 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         uint32_t s_seen0 = 0, s_seen1 = 0;              // phases of s_full[0 / 1] consumed
         uint32_t p_arr0 = 0, p_arr1 = 0;                // phases of p_ready[0 / 1] arrived on
         uint32_t x_use0 = 0, x_use1 = 0;                // accumulations of tile 0 / 1 consumed
-        int it = 0;
-        for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++it) {
+        for (int it = 0;; ++it) {
             if (__any_sync(0xffffffffu, sh.abort_flag != 0)) break;
+            bool qok = true;
+            const int item = queue_read_warp(sh, it, p.status, qok);
+            if (!qok || item >= nitems) break;
             const int t = item / p.npairs, pr = item - t * p.npairs;
             const int ntiles = pr == p.npairs - 1 ? p.tiles_last : 2;
             // lane l holds -lse * log2(e) and -scale * delta of heads l, l + 32, ...
@@ -1072,9 +1137,12 @@ cudaError_t launch_sdi_h(const ChunkArgs& a, cudaStream_t s) {
     sp.tiles_last = (a.R - (sp.npairs - 1) * 256) > 128 ? 2 : 1;
     sp.scale = a.scale; sp.status = a.status;
     sp.qd_mode = qd_mode;
+    sp.work_ctr = sdi_work_counter(a.status);
     const int64_t items = int64_t(a.T) * sp.npairs;
     const int sms = sm_count();
     const int grid = int(items < sms ? items : sms);
+    cudaError_t e = cudaMemsetAsync(sp.work_ctr, 0, sizeof(int), s);
+    if (e != cudaSuccess) return e;
     sdi_kernel<H><<<grid, C::kThreads, C::kSmem, s>>>(mq, mdo, mqda, mqdb, mim, mds, sp);
     note_launch();
     return cudaGetLastError();

@@ -19,6 +19,12 @@ constexpr int kWarp = 32;
 // SMLA_ERR_TIMEOUT). The host clears it at the start of each call.
 constexpr size_t kStatusBytes = 256;
 
+// Byte 64 of the status area: the work counter of the S/dP/dS kernel's
+// dynamic item scheduling, zeroed on the stream before each launch.
+inline int* sdi_work_counter(unsigned* status) {
+    return reinterpret_cast<int*>(reinterpret_cast<char*>(status) + 64);
+}
+
 __device__ __forceinline__ void flag_status(unsigned* status, int code) {
     atomicOr(status, 1u << code);
 }
