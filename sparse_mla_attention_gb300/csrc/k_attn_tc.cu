@@ -60,7 +60,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 #ifdef SMLA_TRACE
 // Optional phase timestamps (compiled only with -DSMLA_TRACE; the library
 // build leaves them out): per kernel, CTA (< 8) and item (< 8), 64 events.
-constexpr int kTraceCtas = 8, kTraceItems = 8, kTraceEvents = 128;
+constexpr int kTraceCtas = 8, kTraceItems = 8, kTraceEvents = 256;
 __device__ unsigned long long g_smla_trace[2 * kTraceCtas * kTraceItems * kTraceEvents];
 // per kernel and CTA (< 1024): start and end time of the CTA's MMA thread
 __device__ unsigned long long g_smla_cta_span[2 * 1024 * 3];
@@ -385,15 +385,16 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 #pragma unroll
         for (int i = 0; i < 32; ++i) idx_nxt[i] = 0;
         const char* kvbase = reinterpret_cast<const char*>(p.kv) + (lane & 7) * 16;
-        // Slots whose copies are issued but not yet signalled. At most kSlots - 2
-        // stay pending, so the next slot to fill never waits for one of them.
-        int pend[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        // Slots whose copies are issued but not yet signalled, oldest in the low
+        // 4 bits (a packed queue: a runtime-indexed array would live in local
+        // memory). At most kSlots - 2 stay pending, so the next slot to fill
+        // never waits for one of them.
+        uint32_t pend = 0;
         int npend = 0;
         auto flush_one = [&]() {
             fence_proxy_async_smem();
-            mbar_arrive(&sh.full[pend[0]]);
-#pragma unroll
-            for (int k = 0; k + 1 < 8; ++k) pend[k] = pend[k + 1];
+            mbar_arrive(&sh.full[pend & 15u]);
+            pend >>= 4;
             --npend;
         };
         int use = 0;              // this CTA's ring use index
@@ -421,7 +422,8 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     }
                 }
                 cp_async_commit();
-                pend[npend++] = slot;
+                pend |= uint32_t(slot) << (4 * npend);
+                ++npend;
                 if (npend == C::kSlots - 1) { cp_async_wait<C::kSlots - 2>(); flush_one(); }
                 if (c == 7) {
                     // signal what is left, then load the next item's indices
@@ -444,9 +446,19 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         if (lane == 0) {
             SMLA_TRACE_SPAN(0, 0);
             int slot = 0; uint32_t phase = 0;
-            uint32_t xe_done[2] = {0, 0};   // drains of tile g's accumulator seen
-            uint32_t x_uses[2] = {0, 0};    // accumulations of tile g issued
-            uint32_t p_seen[2] = {0, 0};    // phases of p_ready[g] waited for
+            // Per tile g (scalars, not arrays: a runtime-indexed array would live in
+            // local memory, and with shared memory taking most of L1 each access
+            // became an L2 round trip on this thread's critical path)
+            uint32_t xe_done0 = 0, xe_done1 = 0;   // drains of tile g's accumulator seen
+            uint32_t x_uses0 = 0, x_uses1 = 0;     // accumulations of tile g issued
+            uint32_t p_seen0 = 0, p_seen1 = 0;     // phases of p_ready[g] waited for
+            auto wait_drains = [&](uint32_t& done, uint32_t uses, uint64_t* bar) -> bool {
+                while (done < uses) {
+                    if (!wait_or_abort(bar, done & 1u, &sh.abort_flag, p.status)) return false;
+                    ++done;
+                }
+                return true;
+            };
             // B-stage slot offsets of the dO blocks (P term) and q blocks (dS term)
             const uint32_t do_off = p.qd_mode == 2 ? 0u : 2u * C::kQBytes;
             const uint32_t q_off = p.qd_mode == 2 ? 2u * C::kQBytes : 0u;
@@ -464,11 +476,8 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     SMLA_TRACE_EV(0, it, 1);
                     // ... and after its drains, which follow the dS stash (the stash
                     // reads P^T / dS^T columns that this A stage overwrites)
-                    for (int g = 0; g < 2 && ok; ++g)
-                        while (ok && xe_done[g] < x_uses[g]) {
-                            ok = wait_or_abort(&sh.x_empty[g], xe_done[g] & 1u, &sh.abort_flag, p.status);
-                            ++xe_done[g];
-                        }
+                    ok = ok && wait_drains(xe_done0, x_uses0, &sh.x_empty[0]);
+                    ok = ok && wait_drains(xe_done1, x_uses1, &sh.x_empty[1]);
                     SMLA_TRACE_EV(0, it, 2);
                 }
                 SMLA_TRACE_EV(0, it, 3);
@@ -497,23 +506,27 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 // g's first step waits for its P / dS, so tile 0's B stage runs while
                 // the epilogue warps work on tile 1.
                 for (int c = 0; c < 4 && ok; ++c) {
+                    SMLA_TRACE_EV(0, it, 144 + c);
                     ok = wait_or_abort(&sh.full[slot], phase, &sh.abort_flag, p.status);
                     SMLA_TRACE_EV(0, it, 16 + c);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t sb = smem_u32(slots + slot * C::kSlotBytes);
-                    for (int g = 0; g < ntiles && ok; ++g) {
+                    // one tile-step of the B stage for tile G (a compile-time constant,
+                    // so that its counters stay in registers)
+                    auto b_step = [&](auto g_tag) -> bool {
+                        constexpr int g = decltype(g_tag)::value;
+                        uint32_t& p_seen = g ? p_seen1 : p_seen0;
+                        uint32_t& xe_done = g ? xe_done1 : xe_done0;
+                        uint32_t& x_uses = g ? x_uses1 : x_uses0;
                         if (c == 0) {
-                            ok = wait_or_abort(&sh.p_ready[g], p_seen[g] & 1u, &sh.abort_flag, p.status);
-                            ++p_seen[g];
-                            if (!ok) break;
+                            if (!wait_or_abort(&sh.p_ready[g], p_seen & 1u, &sh.abort_flag, p.status)) return false;
+                            ++p_seen;
                             if (g == 0) SMLA_TRACE_EV(0, it, 5);
                         }
-                        while (ok && xe_done[g] < x_uses[g]) {
-                            ok = wait_or_abort(&sh.x_empty[g], xe_done[g] & 1u, &sh.abort_flag, p.status);
-                            ++xe_done[g];
-                        }
-                        if (!ok) break;
+                        SMLA_TRACE_EV(0, it, 128 + 2 * c + g);
+                        if (!wait_drains(xe_done, x_uses, &sh.x_empty[g])) return false;
+                        SMLA_TRACE_EV(0, it, 148 + 2 * c + g);
                         tc_fence_after();
                         SMLA_TRACE_EV(0, it, 24 + 2 * c + g);
                         const uint32_t tile = tbase + g * 256;
@@ -527,9 +540,14 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                             mma_ts(tile + 128, tile + acol, sdesc_sw128(bt, C::kQBytes, 1024),
                                    C::kIdescB, ks != 0);
                         }
+                        SMLA_TRACE_EV(0, it, 136 + 2 * c + g);
                         mma_commit(&sh.x_full[g]);
-                        ++x_uses[g];
-                    }
+                        ++x_uses;
+                        return true;
+                    };
+                    ok = b_step(std::integral_constant<int, 0>{});
+                    if (ok && ntiles > 1) ok = b_step(std::integral_constant<int, 1>{});
+                    if (!ok) break;
                     mma_commit(&sh.empty[slot]);
                     if ((8 + c + C::kSlots) % C::kUses < 8) mma_commit(&sh.kempty[slot]);
                     advance(slot, phase, C::kSlots);
@@ -694,6 +712,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             // warps have arrived on the tile's p_ready. It runs after the tile's
             // first drain, under the next MMAs rather than before the drains.
             auto stash = [&](int g2) -> bool {
+                if (lane == 0) SMLA_TRACE_EV(0, it, 224 + (warp - 2) * 4 + 2 * g2);
                 if (grp * 64 >= H) return true;
                 const uint32_t pphase = ((g2 ? p_arr1 : p_arr0) - 1u) & 1u;
                 if (!wait_or_abort_warp(&sh.p_ready[g2], pphase, &sh.abort_flag, p.status)) return false;
@@ -724,6 +743,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     bulk_commit();
                 }
                 __syncwarp();
+                if (lane == 0) SMLA_TRACE_EV(0, it, 224 + (warp - 2) * 4 + 2 * g2 + 1);
                 return true;
             };
             // ---- drain interm columns [128c, 128c + 128) of every tile, tiles
@@ -753,6 +773,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     if (lane == 0) mbar_arrive(&sh.x_empty[g2]);
                     if (lane == 0 && (warp == 2 || warp == 9))
                         SMLA_TRACE_EV(0, it, (warp == 2 ? 64 : 96) + 3 * (2 * c + g2) + 1);
+                    if (lane == 0) SMLA_TRACE_EV(0, it, 160 + (warp - 2) * 8 + 2 * c + g2);
                     if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
                     uint4* srow = reinterpret_cast<uint4*>(stage + lane * 128);
