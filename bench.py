@@ -499,11 +499,11 @@ OVERLAPPED_PHASES = ("csr", "attn_dq", "gather")
 # DRAM traffic per launch of the dominant kernels, from one ncu capture (see
 # profiles/), valid only while the kernel source is the one captured.
 _NCU_TRAFFIC = {
-    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "e756570005956a5d"),
-                 "bytes_per_token": (141.009920e6 + 274.377728e6) / 512,
+    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "8064850532842318"),
+                 "bytes_per_token": (139.401728e6 + 275.856896e6) / 512,
                  "note": "ncu capture of the first 512 tokens, scaled by tokens"},
-    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "e756570005956a5d"),
-                "bytes_per_token": (69.773312e6 + 15.686400e6) / 512,
+    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "8064850532842318"),
+                "bytes_per_token": (69.763328e6 + 17.347328e6) / 512,
                 "note": "ncu capture of the first 512 tokens, scaled by tokens"},
     "fwd_tc": {"sources": ("sparse_mla_attention_gb300/csrc/k_fwd_tc.cu", "9782f171a5790295"),
                "bytes_per_token": (72.783872e6 + 17.696512e6) / 512,
