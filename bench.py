@@ -461,6 +461,12 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_oracle_sample(spec, inp, seconds=args.cpu_seconds)
 
+    # ---- the other configurations of the workload table, timed the same way
+    # (after the headline's timed region; one GPU only)
+    others = None
+    if world == 1 and not args.no_configs and not args.tokens and args.workload == WORKLOAD:
+        others = _other_configs(dev, peaks, steps=max(10, args.steps // 5), warmup=3)
+
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -480,6 +486,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "forward": fwd,
+        "other_configs": others,
         "gpu_launches": launches,
         "clocks": clk,
         "pages_context": PAGES_CONTEXT,
@@ -489,6 +496,58 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def _other_configs(dev, peaks, steps: int, warmup: int) -> dict:
+    """ms per backward call (median, p10, p90 of `steps` calls) and valid TFLOP/s
+    of the workload table's other large configurations: H=64 with four rank
+    chunks of 128, and T=8192 with Zipf pool picks and 30 % masked ranks."""
+    import numpy as np
+    import torch
+    import sparse_mla_attention_gb300 as smla
+    from sparse_mla_attention_gb300 import workloads as W
+    res = {}
+    stream = torch.cuda.current_stream(dev)
+    for name in ("headline_h64_chunked", "t8192_zipf"):
+        spec = W.WORKLOADS[name]
+        inp = W.make_inputs(spec)
+
+        def up(bits):
+            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        q, kv, do = (up(inp[k]) for k in ("q", "kv", "do"))
+        topk = torch.from_numpy(inp["topk"]).to(dev)
+        sink = None if inp["sink"] is None else torch.from_numpy(inp["sink"]).to(dev)
+        o, lse = smla.sparse_mla_fwd(q, kv, topk, sink, scale=inp["scale"])
+        ws = smla.Workspace(dev)
+        out = (torch.empty_like(q), torch.empty_like(kv),
+               None if sink is None else torch.empty(spec.H, dtype=torch.float32, device=dev))
+
+        def step():
+            smla.sparse_mla_bwd(q, kv, do, o, lse, topk, sink, scale=inp["scale"],
+                                r_chunk=spec.r_chunk or None, workspace=ws, out=out, check_status=False)
+
+        step()
+        if smla.device_status(ws.buf) != 0:
+            raise RuntimeError(f"device status set by the {name} backward")
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        evs[0].record(stream)
+        for i in range(steps):
+            step()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        calls = _percentiles(evs[i].elapsed_time(evs[i + 1]) for i in range(steps))
+        flops = W.flops_valid(inp["topk"], spec.H)
+        tf = flops / (calls["median"] * 1e-3) / 1e12
+        res[name] = {"shape": spec.describe(), "per_call_ms": calls, "flops_valid_per_call": flops,
+                     "tflops_valid": tf, "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+                     "peak_source": peaks["source"] + " bf16 burst"}
+        del q, kv, do, topk, sink, o, lse, ws, out
+        torch.cuda.empty_cache()
+    return res
 
 
 # Phases that run concurrently with others (the CSR build and dq on the
@@ -557,6 +616,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fwd", action="store_true", help="skip the separate forward timing")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the other configurations (H=64 chunked, T=8192 Zipf)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--tokens", type=int, default=0,
                     help="time only the first N tokens of the workload (small profiling cases)")
