@@ -371,13 +371,17 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int rl = pr * 256 + 8 * i + 4 * gw + (lane >> 3);
-                int j = 0;
+                // masked, invalid, or past the chunk's end: any real row will do
+                // (P of that rank is zeroed), but not one fixed row, which every
+                // CTA would then read at once: the slot's own rank position
+                // spreads them over up to 512 rows (the zero-filling form of
+                // cp.async, and a modulo here, both measured slower)
+                int j = -1;
                 if (rl < p.R) {
                     j = __ldg(p.topk + int64_t(t) * p.K + p.r0 + rl);
-                    if (j < -1 || j >= p.N) { flag_status(p.status, SMLA_ERR_INDEX); j = 0; }
-                    if (j < 0) j = 0;              // masked: any real row; its P is zeroed
+                    if (j < -1 || j >= p.N) { flag_status(p.status, SMLA_ERR_INDEX); j = -1; }
                 }
-                out[i] = j;
+                out[i] = j >= 0 ? j : (rl < p.N ? rl : 0);
             }
         };
         int cur = queue_read_warp(sh, 0, p.status, ok);
@@ -926,14 +930,15 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
         const int my_items =
             int(blockIdx.x) < nitems ? (nitems - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
         const int nchunks = my_items * nkc;
+        // -1 (masked, invalid or past the chunk's end): zeros instead of a copy
         auto load_idx = [&](int n) -> int {
-            if (n >= nchunks) return 0;
+            if (n >= nchunks) return -1;
             const int item = blockIdx.x + (n / nkc) * int(gridDim.x);
             const int rl = (n % nkc) * 64 + 16 * wt + (lane & 15);
-            int j = 0;
+            int j = -1;
             if (rl < p.R) {
                 j = __ldg(p.topk + int64_t(item >> 1) * p.K + p.r0 + rl);
-                if (j < 0 || j >= p.N) j = 0;      // masked or invalid: its dS is zero
+                if (j < 0 || j >= p.N) j = -1;     // masked or invalid: its dS is zero
             }
             return j;
         };
@@ -953,10 +958,11 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
             for (int qd = 0; qd < 4; ++qd) {
                 const int r = 16 * wt + 4 * qd + rq;
                 const int j = __shfl_sync(0xffffffffu, idx, 4 * qd + rq);
-                const char* src = src0 + int64_t(j) * (kD * 2);
+                const char* src = src0 + int64_t(j < 0 ? 0 : j) * (kD * 2);
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
-                    cp_async16(sbase + b * 8192 + r * 128 + ((piece ^ (r & 7)) << 4), src + b * 128);
+                    cp_async16_zfill(sbase + b * 8192 + r * 128 + ((piece ^ (r & 7)) << 4), src + b * 128,
+                                     j < 0 ? 0u : 16u);
             }
             cp_async_commit();
             cp_async_wait<0>();

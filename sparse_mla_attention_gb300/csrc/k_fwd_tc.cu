@@ -132,11 +132,20 @@ __device__ __forceinline__ int ft_raw(const FtParams& p, int t, int r) {
     return r < p.K ? __ldg(p.topk + int64_t(t) * p.K + r) : -1;
 }
 
-// Row to copy for a raw index (row 0 for a masked or invalid one); `bad`
-// collects indices outside [-1, N).
+// Row to copy for a raw index, or -1 for a masked or invalid one (its smem row
+// is zero-filled instead: copying one placeholder row for every masked slot
+// would send every CTA to the same L2 lines); `bad` collects indices outside
+// [-1, N).
 __device__ __forceinline__ int ft_row_of(int j, int N, bool& bad) {
     bad |= (j < -1) | (j >= N);
-    return (j >= 0 && j < N) ? j : 0;
+    return (j >= 0 && j < N) ? j : -1;
+}
+
+// One 16-byte piece of a kv row into shared memory: `src` is the piece's
+// address in row `row`, or in row 0 for a masked slot (row < 0), whose piece
+// is zero-filled without reading global memory.
+__device__ __forceinline__ void ft_copy_piece(void* dst, const char* src, int row) {
+    cp_async16_zfill(dst, src, row < 0 ? 0u : 16u);
 }
 
 }  // namespace
@@ -261,8 +270,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                 for (int i = 0; i < 16; ++i) {
                     const int rl = 4 * i + (lane >> 3);              // row within the warp's 64
                     const int row = __shfl_sync(0xffffffffu, i < 8 ? c0 : c1, rl & 31);
-                    cp_async16(sb + (64 * wt + rl) * 128 + ((piece ^ (rl & 7)) << 4),
-                               kvb + int64_t(row) * (kD * 2) + c * 128 + piece * 16);
+                    ft_copy_piece(sb + (64 * wt + rl) * 128 + ((piece ^ (rl & 7)) << 4),
+                                  kvb + int64_t(row < 0 ? 0 : row) * (kD * 2) + c * 128 + piece * 16, row);
                 }
             } else {
                 const int c = (u - 8 * nt2) / nt;
@@ -270,11 +279,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                 for (int i = 0; i < 8; ++i) {
                     const int rl = 4 * i + (lane >> 3);              // row within the warp's 32
                     const int row = __shfl_sync(0xffffffffu, c0, rl);
-                    const char* src = kvb + int64_t(row) * (kD * 2) + c * 256 + piece * 16;
+                    const char* src = kvb + int64_t(row < 0 ? 0 : row) * (kD * 2) + c * 256 + piece * 16;
 #pragma unroll
                     for (int blk = 0; blk < 2; ++blk)
-                        cp_async16(sb + blk * 16384 + (32 * wt + rl) * 128 + ((piece ^ (rl & 7)) << 4),
-                                   src + blk * 128);
+                        ft_copy_piece(sb + blk * 16384 + (32 * wt + rl) * 128 + ((piece ^ (rl & 7)) << 4),
+                                      src + blk * 128, row);
                 }
             }
             cp_async_commit();
