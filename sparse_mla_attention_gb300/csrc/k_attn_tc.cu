@@ -154,8 +154,24 @@ struct SdiParams {
     // the S^T | dP^T accumulator and the first half of each B-stage slot.
     int qd_mode;
     int* work_ctr;        // next work item (zeroed before the launch)
+    // with cnt set, topk is a compacted table (each token's valid entries
+    // first) and cnt[t] their number: a token has ceil(cnt / 128) tiles (at
+    // least one), so masked slots cost no tensor work
+    const int32_t* cnt;
     unsigned* status;
 };
+
+// Tiles (0, 1 or 2) of work item `item` = (token, 256-rank pair).
+__device__ __forceinline__ int sdi_ntiles(const SdiParams& p, int item) {
+    const int t = item / p.npairs, pr = item - t * p.npairs;
+    if (p.cnt) {
+        int m = __ldg(p.cnt + t);
+        if (m < 1) m = 1;              // one all-masked tile: the stash rows dq reads are written
+        const int n = ((m + 127) >> 7) - 2 * pr;
+        return n < 0 ? 0 : (n > 2 ? 2 : n);
+    }
+    return pr == p.npairs - 1 ? p.tiles_last : 2;
+}
 
 struct SdiShared {
     uint64_t full[8], empty[8];
@@ -167,9 +183,10 @@ struct SdiShared {
     uint64_t kempty[8];
     uint64_t s_full[2], p_ready[2], x_full[2], x_empty[2], b_done[2], drain;
     // Work queue: the TMA thread takes items from the global counter and
-    // publishes them in order; every other role reads entry k for its k-th
-    // item (the copy warps one item ahead). An entry >= the item count ends
-    // the CTA's work. CTAs that start late (their SM still busy with another
+    // publishes them in order, as item * 4 + its tile count (so that no other
+    // role loads the count); every other role reads entry k for its k-th item
+    // (the copy warps one item ahead). An item >= the item count ends the
+    // CTA's work. CTAs that start late (their SM still busy with another
     // kernel) simply take fewer items.
     int item_q[4];
     uint64_t q_full[4], q_empty[4];
@@ -179,7 +196,8 @@ struct SdiShared {
 
 constexpr int kQueueReaders = 11;   // 2 copy warps + the MMA thread + 8 epilogue warps
 
-// Entry k of the work queue, read by a whole warp (lane 0 signals the read).
+// Entry k of the work queue (item * 4 + tiles), read by a whole warp (lane 0
+// signals the read).
 __device__ __forceinline__ int queue_read_warp(SdiShared& sh, int k, unsigned* status, bool& ok) {
     const int e = k & 3;
     if (!wait_or_abort_warp(&sh.q_full[e], uint32_t(k >> 2) & 1u, &sh.abort_flag, status)) {
@@ -192,7 +210,7 @@ __device__ __forceinline__ int queue_read_warp(SdiShared& sh, int k, unsigned* s
     return item;
 }
 
-// Entry k of the work queue, read by one thread.
+// Entry k of the work queue (item * 4 + tiles), read by one thread.
 __device__ __forceinline__ int queue_read_thread(SdiShared& sh, int k, unsigned* status, bool& ok) {
     const int e = k & 3;
     if (!wait_or_abort(&sh.q_full[e], uint32_t(k >> 2) & 1u, &sh.abort_flag, status)) {
@@ -295,9 +313,10 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 if (pub >= 4 &&
                     !wait_or_abort(&sh.q_empty[e], uint32_t((pub >> 2) - 1) & 1u, &sh.abort_flag, p.status))
                     return false;
-                int item = atomicAdd(p.work_ctr, 1);
+                int item = atomicAdd(p.work_ctr, 1), nt = 0;
+                while (item < nitems && (nt = sdi_ntiles(p, item)) == 0) item = atomicAdd(p.work_ctr, 1);
                 if (item > nitems) item = nitems;
-                sh.item_q[e] = item;
+                sh.item_q[e] = item * 4 + (item < nitems ? nt : 0);
                 mbar_arrive(&sh.q_full[e]);
                 last = item;
                 ++pub;
@@ -306,7 +325,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             ok = publish();
             if (ok && last < nitems) ok = publish();
             for (int it = 0; ok; ++it) {
-                const int item = sh.item_q[it & 3];
+                const int item = sh.item_q[it & 3] >> 2;
                 if (item >= nitems) break;
                 // entry it + 2 (the copy warps read entry it + 1 during this item)
                 if (last < nitems && !publish()) { ok = false; break; }
@@ -384,7 +403,8 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 out[i] = j >= 0 ? j : (rl < p.N ? rl : 0);
             }
         };
-        int cur = queue_read_warp(sh, 0, p.status, ok);
+        int ecur = queue_read_warp(sh, 0, p.status, ok);
+        int cur = ecur >> 2;
         if (cur < nitems) load_idx(cur, idx_cur);
 #pragma unroll
         for (int i = 0; i < 32; ++i) idx_nxt[i] = 0;
@@ -404,9 +424,8 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         int use = 0;              // this CTA's ring use index
         uint32_t kph = 0;         // per slot: parity of its next kempty phase
         for (int k = 0; ok && cur < nitems; ++k) {
-            const int pr = cur % p.npairs;
-            const int ntiles = pr == p.npairs - 1 ? p.tiles_last : 2;
-            int nxt = nitems;
+            const int ntiles = ecur & 3;
+            int enxt = nitems * 4;
             for (int c = 0; c < 8; ++c, ++use) {
                 if (use >= C::kSlots) {   // the slot's previous use must be consumed
                     if (lane == 0)
@@ -433,8 +452,8 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     // signal what is left, then load the next item's indices
                     cp_async_wait<0>();
                     while (npend > 0) flush_one();
-                    nxt = queue_read_warp(sh, k + 1, p.status, ok);
-                    if (nxt < nitems) load_idx(nxt, idx_nxt);
+                    enxt = queue_read_warp(sh, k + 1, p.status, ok);
+                    if ((enxt >> 2) < nitems) load_idx(enxt >> 2, idx_nxt);
                 }
                 advance(slot, phase, C::kSlots);
             }
@@ -442,7 +461,8 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             for (int u = 8; u < C::kUses; ++u, ++use) advance(slot, phase, C::kSlots);
 #pragma unroll
             for (int i = 0; i < 32; ++i) idx_cur[i] = idx_nxt[i];
-            cur = nxt;
+            ecur = enxt;
+            cur = ecur >> 2;
         }
         cp_async_wait<0>();
     } else if (warp == 1) {
@@ -468,10 +488,10 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             const uint32_t q_off = p.qd_mode == 2 ? 2u * C::kQBytes : 0u;
             bool ok = true;
             for (int it = 0; ok; ++it) {
-                const int item = queue_read_thread(sh, it, p.status, ok);
+                const int ent = queue_read_thread(sh, it, p.status, ok);
+                const int item = ent >> 2;
                 if (!ok || item >= nitems) break;
-                const int pr = item % p.npairs;
-                const int ntiles = pr == p.npairs - 1 ? p.tiles_last : 2;
+                const int ntiles = ent & 3;
                 // A stage may overwrite TMEM only after the previous item's B stage
                 // read P / dS ...
                 if (it > 0) {
@@ -595,10 +615,11 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         for (int it = 0;; ++it) {
             if (__any_sync(0xffffffffu, sh.abort_flag != 0)) break;
             bool qok = true;
-            const int item = queue_read_warp(sh, it, p.status, qok);
+            const int ent = queue_read_warp(sh, it, p.status, qok);
+            const int item = ent >> 2;
             if (!qok || item >= nitems) break;
             const int t = item / p.npairs, pr = item - t * p.npairs;
-            const int ntiles = pr == p.npairs - 1 ? p.tiles_last : 2;
+            const int ntiles = ent & 3;
             // lane l holds -lse * log2(e) and -scale * delta of heads l, l + 32, ...
             float lse_w[kHw], del_w[kHw];
 #pragma unroll
@@ -831,8 +852,18 @@ struct DqParams {
     uint16_t* dq_out;     // bf16 [T, H, 512]
     int T, K, N, r0, R, Rp;
     bool first, last;
+    const int32_t* cnt;   // compacted table: valid entries per token (see SdiParams), or nullptr
     unsigned* status;
 };
+
+// 64-rank chunks of token t: all Rp / 64, or with a compacted table those
+// holding its valid entries (at least one: an all-masked token's dq is the
+// product of its zero dS rows).
+__device__ __forceinline__ int dq_nchunks(const DqParams& p, int t, int nkc) {
+    if (!p.cnt) return nkc;
+    const int m = __ldg(p.cnt + t);
+    return m < 1 ? 1 : (m + 63) >> 6;
+}
 
 struct DqShared {
     uint64_t full[4], empty[4];
@@ -892,10 +923,15 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
             int slot = 0; uint32_t phase = 0; int issued = 0;
             bool ok = true;
             int it = 0;
+            // chunk counts are loaded one item ahead (off this thread's critical path)
+            int nk_next = int(blockIdx.x) < nitems ? dq_nchunks(p, int(blockIdx.x) >> 1, nkc) : 0;
             for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
                 const int t = item >> 1;
+                const int nk = nk_next;
+                const int later = item + int(gridDim.x);
+                nk_next = later < nitems ? dq_nchunks(p, later >> 1, nkc) : 0;
                 SMLA_TRACE_EV(1, it, 0);
-                for (int kc = 0; kc < nkc; ++kc) {
+                for (int kc = 0; kc < nk; ++kc) {
                     ok = wait_or_abort(&sh.empty[slot], phase ^ 1u, &sh.abort_flag, p.status);
                     if (!ok) break;
                     uint8_t* sb = slots + slot * kDqSlotBytes;
@@ -927,24 +963,35 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
         const int gw = warp - 6;
         const int team = gw / kDqTeamWarps, wt = gw % kDqTeamWarps;
         const int rq = lane >> 3, piece = lane & 7;
-        const int my_items =
-            int(blockIdx.x) < nitems ? (nitems - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
-        const int nchunks = my_items * nkc;
-        // -1 (masked, invalid or past the chunk's end): zeros instead of a copy
-        auto load_idx = [&](int n) -> int {
-            if (n >= nchunks) return -1;
-            const int item = blockIdx.x + (n / nkc) * int(gridDim.x);
-            const int rl = (n % nkc) * 64 + 16 * wt + (lane & 15);
+        // The CTA's chunk sequence: its items blockIdx.x, blockIdx.x + gridDim.x,
+        // ..., each of dq_nchunks 64-rank chunks; chunk n of the sequence sits in
+        // slot n % kDqSlots and is filled by team n % kDqTeams.
+        // (nk: the cursor item's chunk count, loaded once per item)
+        struct Cursor { int item, kc, nk; };
+        auto step = [&](Cursor& c) {
+            if (c.item >= nitems) return;
+            if (++c.kc == c.nk) {
+                c.kc = 0;
+                c.item += int(gridDim.x);
+                c.nk = c.item < nitems ? dq_nchunks(p, c.item >> 1, nkc) : 0;
+            }
+        };
+        auto load_idx = [&](const Cursor& c) -> int {
+            if (c.item >= nitems) return -1;
+            const int rl = c.kc * 64 + 16 * wt + (lane & 15);
             int j = -1;
             if (rl < p.R) {
-                j = __ldg(p.topk + int64_t(item >> 1) * p.K + p.r0 + rl);
+                j = __ldg(p.topk + int64_t(c.item >> 1) * p.K + p.r0 + rl);
                 if (j < 0 || j >= p.N) j = -1;     // masked or invalid: its dS is zero
             }
             return j;
         };
-        int idx = load_idx(team);
-        for (int n = team; n < nchunks; n += kDqTeams) {
-            const int item = blockIdx.x + (n / nkc) * int(gridDim.x);
+        Cursor cur{int(blockIdx.x), 0,
+                   int(blockIdx.x) < nitems ? dq_nchunks(p, int(blockIdx.x) >> 1, nkc) : 0};
+        for (int k = 0; k < team; ++k) step(cur);
+        int idx = load_idx(cur);
+        for (int n = team; cur.item < nitems; n += kDqTeams) {
+            const int item = cur.item;
             const int slot = n % kDqSlots;
             const uint32_t phase = uint32_t(n / kDqSlots) & 1u;
             uint8_t* sbase = slots + slot * kDqSlotBytes + kDqABytes;
@@ -952,7 +999,9 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
             if (lane == 0) ok = wait_or_abort(&sh.empty[slot], phase ^ 1u, &sh.abort_flag, p.status);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
-            const int nxt = load_idx(n + kDqTeams);
+            Cursor nx = cur;
+            for (int k = 0; k < kDqTeams; ++k) step(nx);
+            const int nxt = load_idx(nx);
             const char* src0 = reinterpret_cast<const char*>(p.kv) + (item & 1) * 512 + piece * 16;
 #pragma unroll
             for (int qd = 0; qd < 4; ++qd) {
@@ -969,6 +1018,7 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
             fence_proxy_async_smem();
             mbar_arrive(&sh.full[slot]);
             idx = nxt;
+            cur = nx;
         }
         cp_async_wait<0>();
     } else if (warp == 1) {
@@ -978,11 +1028,15 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
             int slot = 0; uint32_t phase = 0;
             bool ok = true;
             int it = 0;
+            int nk_next = int(blockIdx.x) < nitems ? dq_nchunks(p, int(blockIdx.x) >> 1, nkc) : 0;
             for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
                 const int b = it & 1;
+                const int nk = nk_next;
+                const int later = item + int(gridDim.x);
+                nk_next = later < nitems ? dq_nchunks(p, later >> 1, nkc) : 0;
                 if (it >= 2) ok = wait_or_abort(&sh.d_empty[b], ((it >> 1) - 1) & 1, &sh.abort_flag, p.status);
                 SMLA_TRACE_EV(1, it, 2);
-                for (int kc = 0; kc < nkc && ok; ++kc) {
+                for (int kc = 0; kc < nk && ok; ++kc) {
                     ok = wait_or_abort(&sh.full[slot], phase, &sh.abort_flag, p.status);
                     if (!ok) break;
                     tc_fence_after();
@@ -1165,6 +1219,7 @@ cudaError_t launch_sdi_h(const ChunkArgs& a, cudaStream_t s) {
     sp.scale = a.scale; sp.status = a.status;
     sp.qd_mode = qd_mode;
     sp.work_ctr = sdi_work_counter(a.status);
+    sp.cnt = a.cnt;
     const int64_t items = int64_t(a.T) * sp.npairs;
     const int sms = sm_count();
     const int grid = int(items < sms ? items : sms);
@@ -1188,6 +1243,7 @@ cudaError_t launch_dq_h(const ChunkArgs& a, cudaStream_t s) {
     dp.kv = a.kv; dp.topk = a.topk; dp.dq_acc = a.dq_acc; dp.dq_out = a.dq_out;
     dp.T = a.T; dp.K = a.K; dp.N = a.N; dp.r0 = a.r0; dp.R = a.R; dp.Rp = Rp;
     dp.first = a.first_chunk; dp.last = a.last_chunk; dp.status = a.status;
+    dp.cnt = a.cnt;
     const int64_t items = int64_t(a.T) * 2;
     // dq runs beside the dKV gather (another stream). Each dq CTA's throughput
     // is fixed by its own copy pipeline, while the gather speeds up with every

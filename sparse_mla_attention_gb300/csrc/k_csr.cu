@@ -39,6 +39,51 @@ __device__ __forceinline__ void load_entry(const KeySource& src, int64_t e, int&
     }
 }
 
+// One warp per token row, in batches of 512 entries: each lane loads its 16
+// entries of the batch first (independent loads, one memory latency per
+// batch), then 16 ballots of the valid ones give each its place among the
+// row's valid entries so far.
+__global__ void __launch_bounds__(256) compact_ranks_kernel(const int32_t* __restrict__ topk, int T, int K,
+                                                             int num_kv, int32_t* __restrict__ cidx,
+                                                             int32_t* __restrict__ cnt, unsigned* status) {
+    const int lane = threadIdx.x & 31;
+    const int t = int((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+    if (t >= T) return;
+    const int32_t* row = topk + int64_t(t) * K;
+    int32_t* out = cidx + int64_t(t) * K;
+    const unsigned lt = (1u << lane) - 1u;
+    int base = 0;
+    for (int b0 = 0; b0 < K; b0 += 512) {
+        int j[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int r = b0 + 32 * k + lane;
+            j[k] = r < K ? __ldg(row + r) : -1;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (j[k] < -1 || j[k] >= num_kv) {
+                flag_status(status, SMLA_ERR_INDEX);
+                j[k] = -1;
+            }
+            const unsigned v = __ballot_sync(0xffffffffu, j[k] >= 0);
+            if (j[k] >= 0) out[base + __popc(v & lt)] = j[k];
+            base += __popc(v);
+        }
+    }
+    for (int r = base + lane; r < K; r += 32) out[r] = -1;
+    if (lane == 0) cnt[t] = base;
+}
+
+cudaError_t launch_compact_ranks(const int32_t* topk, int T, int K, int num_kv, int32_t* cidx,
+                                 int32_t* cnt, unsigned* status, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    const int64_t blocks = (int64_t(T) + 7) / 8;     // 8 warps, one per token
+    compact_ranks_kernel<<<unsigned(blocks), 256, 0, s>>>(topk, T, K, num_kv, cidx, cnt, status);
+    note_launch();
+    return cudaGetLastError();
+}
+
 CsrPlan plan_csr(int64_t T, int64_t r_len, int64_t num_kv) {
     CsrPlan p{};
     p.n = T * r_len;

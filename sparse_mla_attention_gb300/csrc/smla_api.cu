@@ -84,6 +84,12 @@ BwdPlan plan_bwd(const smla_dims& d) {
     // With rank chunks of a multiple of 128 ranks the dS^T stash covers all ranks
     // and dq runs once after the last chunk (no fp32 dq accumulator).
     p.full_stash = p.nchunks > 1 && p.R % 128 == 0;
+    // Unchunked calls compact each token's valid ranks to the front of its row:
+    // masked slots then cost no tensor work, and CSR positions are compacted
+    // positions (the interm rows the S/dP/dS kernel writes).
+    p.compact = p.nchunks == 1;
+    p.off_cidx = take(p.compact ? size_t(p.T * p.K) * 4 : 0);
+    p.off_ccnt = take(p.compact ? size_t(p.T) * 4 : 0);
     const int64_t ds_rows = p.full_stash ? p.K : round_up_ranks(int(p.R));
     p.off_dst = take(size_t(p.T) * ds_rows * pad_heads(int(p.H)) * 2);
     p.off_dqacc = take(p.nchunks > 1 && !p.full_stash ? size_t(p.T * p.H) * kD * 4 : 0);
@@ -267,17 +273,27 @@ int enqueue_bwd(const BwdArgs& A, const smla_dims& d, const BwdPlan& plan, char*
     SideStream* side = side_stream();
     if (!side) return SMLA_ERR_CUDA;
     const float scale = eff_scale(d);
+    int32_t* cidx = plan.compact ? reinterpret_cast<int32_t*>(ws + plan.off_cidx) : nullptr;
+    int32_t* ccnt = plan.compact ? reinterpret_cast<int32_t*>(ws + plan.off_ccnt) : nullptr;
     for (int c = 0; c < plan.nchunks; ++c) {
         const int r0 = int(c * plan.R);
         const bool first = c == 0, last = c == plan.nchunks - 1;
+        // the compacted table, on this stream before delta: the S/dP/dS and dq
+        // kernels and the CSR read it (on the side stream it waited for delta's
+        // blocks, which fill the SMs)
+        if (plan.compact) {
+            prof::Scope ph(prof::kCsr, s);
+            rc = cuda_rc(launch_compact_ranks(A.topk, d.T, d.topk, d.num_kv, cidx, ccnt, status, s));
+            if (rc) return rc;
+        }
         // CSR of this chunk on the side stream (after the previous chunk's gather,
         // which read the CSR buffers); joined back before this chunk's gather
         if ((rc = cuda_rc(cudaEventRecord(side->fork, s)))) return rc;
         if ((rc = cuda_rc(cudaStreamWaitEvent(side->stream, side->fork, 0)))) return rc;
         {
             prof::Scope ph(prof::kCsr, side->stream);
-            rc = cuda_rc(launch_csr(A.topk, d.T, d.topk, r0, int(plan.R), d.num_kv, row_ptr, col,
-                                    ws + plan.off_csr, plan.csr, status, side->stream));
+            rc = cuda_rc(launch_csr(plan.compact ? cidx : A.topk, d.T, d.topk, r0, int(plan.R), d.num_kv,
+                                    row_ptr, col, ws + plan.off_csr, plan.csr, status, side->stream));
             if (rc) return rc;
         }
         if ((rc = cuda_rc(cudaEventRecord(side->join, side->stream)))) return rc;
@@ -293,7 +309,9 @@ int enqueue_bwd(const BwdArgs& A, const smla_dims& d, const BwdPlan& plan, char*
             }
             ChunkArgs a{};
             a.q = A.q + th * kD; a.kv = A.kv; a.dO = A.dO + th * kD; a.lse = A.lse + th;
-            a.delta = delta + th; a.topk = A.topk + int64_t(t0) * d.topk;
+            a.delta = delta + th;
+            a.topk = (plan.compact ? cidx : A.topk) + int64_t(t0) * d.topk;
+            a.cnt = plan.compact ? ccnt + t0 : nullptr;
             a.T = t1 - t0; a.H = d.H; a.K = d.topk; a.N = d.num_kv; a.r0 = r0; a.R = int(plan.R);
             a.scale = scale;
             a.interm = interm + int64_t(t0) * plan.R * kD;

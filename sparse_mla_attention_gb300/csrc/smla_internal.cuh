@@ -89,10 +89,11 @@ struct BwdPlan {
     int64_t T, H, K, N, R;   // R = rank chunk
     int nchunks;
     bool full_stash;         // chunked, R a multiple of 128: one dS^T stash of all ranks
+    bool compact;            // unchunked: the kernels read a compacted index table (below)
     CsrPlan csr;
     int64_t max_segs;
     size_t off_delta, off_rowptr, off_col, off_csr, off_segptr, off_segrow, off_segcnt,
-        off_scan_tmp2, off_partial, off_interm, off_dst, off_dqacc, off_dkvacc;
+        off_scan_tmp2, off_partial, off_interm, off_dst, off_dqacc, off_dkvacc, off_cidx, off_ccnt;
     size_t bytes;
 };
 
@@ -118,6 +119,11 @@ cudaError_t launch_reduce_partials(const float* partials, int n_parts, int64_t n
                                    uint16_t* out_bf16, float* out_f32, cudaStream_t s);
 cudaError_t launch_exclusive_scan(const int32_t* in, int32_t* out, int64_t n,
                                   void* tmp, cudaStream_t s, bool write_total);
+// Compacted index table: row t of `cidx` [T, K] holds the valid entries of
+// topk row t (0 <= j < num_kv), in rank order, then -1; cnt[t] = their number.
+// Indices outside [-1, num_kv) set SMLA_ERR_INDEX and count as masked.
+cudaError_t launch_compact_ranks(const int32_t* topk, int T, int K, int num_kv, int32_t* cidx,
+                                 int32_t* cnt, unsigned* status, cudaStream_t s);
 cudaError_t launch_csr(const int32_t* topk, int T, int topk_w, int r0, int r_len, int num_kv,
                        int32_t* row_ptr, int32_t* col, char* scratch, const CsrPlan& p,
                        unsigned* status, cudaStream_t s);
@@ -143,6 +149,9 @@ cudaError_t launch_fwd_tc(const uint16_t* q, const uint16_t* kv, const int32_t* 
 struct ChunkArgs {
     const uint16_t* q; const uint16_t* kv; const uint16_t* dO;
     const float* lse; const float* delta; const int32_t* topk;
+    // with `cnt` set, topk is a compacted table (valid entries first, then -1)
+    // and cnt[t] the number of valid entries of token t
+    const int32_t* cnt;
     int T, H, K, N, r0, R;
     float scale;
     uint16_t* interm; uint16_t* dsT;
