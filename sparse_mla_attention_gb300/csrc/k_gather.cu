@@ -29,13 +29,17 @@ __global__ void seg_fill(const int32_t* __restrict__ seg_ptr, int num_kv,
 }
 
 // One warp per (segment, half of D); lane l owns 8 consecutive columns
-// (one 16-byte load per contributor).
+// (one 16-byte load per contributor). The segment's contributor positions
+// are loaded first, 8 per lane (one coalesced load each), and handed out by
+// shuffles, so the interm loads do not wait on position loads; 8 interm loads
+// per lane are in flight at a time. The additions run in CSR order.
 __global__ void __launch_bounds__(256) seg_sum(const int32_t* __restrict__ row_ptr,
                                                const int32_t* __restrict__ col,
                                                const uint4* __restrict__ interm,
                                                const int32_t* __restrict__ seg_ptr,
                                                const int32_t* __restrict__ seg_row, int num_kv,
                                                float4* __restrict__ partial) {
+    static_assert(kGatherSeg == 256, "a segment is 8 rounds of 32 positions");
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t sidx = gw >> 1;
@@ -45,33 +49,41 @@ __global__ void __launch_bounds__(256) seg_sum(const int32_t* __restrict__ row_p
     const int local = int(sidx - seg_ptr[j]);
     const int e0 = row_ptr[j] + local * kGatherSeg;
     const int e1 = min(e0 + kGatherSeg, row_ptr[j + 1]);
+    const int n = e1 - e0;
+    int cl[8];                                    // cl[k] on lane l: position e0 + 32k + l
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int ee = e0 + 32 * k + lane;
+        cl[k] = ee < e1 ? __ldg(col + ee) : 0;
+    }
     float acc[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) acc[k] = 0.f;
     constexpr int kRowVec = kD * 2 / 16;          // 64 uint4 per interm row
     const int vcol = half * 32 + lane;
-    int e = e0;
-    for (; e + 4 <= e1; e += 4) {
-        uint4 v[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = __ldg(interm + int64_t(col[e + u]) * kRowVec + vcol);
+    for (int k = 0; k < 8; ++k) {
+        if (32 * k >= n) break;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint32_t* x = reinterpret_cast<const uint32_t*>(&v[u]);
+        for (int b = 0; b < 32; b += 8) {
+            if (32 * k + b >= n) break;
+            uint4 v[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                acc[2 * k] += bf16_lo(x[k]);
-                acc[2 * k + 1] += bf16_hi(x[k]);
+            for (int u = 0; u < 8; ++u) {
+                const int pos = __shfl_sync(0xffffffffu, cl[k], b + u);
+                v[u] = 32 * k + b + u < n ? __ldg(interm + int64_t(pos) * kRowVec + vcol)
+                                          : make_uint4(0u, 0u, 0u, 0u);
             }
-        }
-    }
-    for (; e < e1; ++e) {
-        const uint4 v = __ldg(interm + int64_t(col[e]) * kRowVec + vcol);
-        const uint32_t* x = reinterpret_cast<const uint32_t*>(&v);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            acc[2 * k] += bf16_lo(x[k]);
-            acc[2 * k + 1] += bf16_hi(x[k]);
+            for (int u = 0; u < 8; ++u) {
+                if (32 * k + b + u >= n) break;
+                const uint32_t* x = reinterpret_cast<const uint32_t*>(&v[u]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[2 * q] += bf16_lo(x[q]);
+                    acc[2 * q + 1] += bf16_hi(x[q]);
+                }
+            }
         }
     }
     float4* out = partial + sidx * (kD / 4) + half * 64 + lane * 2;
