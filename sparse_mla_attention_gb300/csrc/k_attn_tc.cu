@@ -158,11 +158,16 @@ struct SdiParams {
     // first) and cnt[t] their number: a token has ceil(cnt / 128) tiles (at
     // least one), so masked slots cost no tensor work
     const int32_t* cnt;
+    // two-token items (heads <= 64, at most 128 ranks per token): item i holds
+    // tokens 2i and 2i + 1, one 128-rank tile each
+    int tt;
     unsigned* status;
 };
 
-// Tiles (0, 1 or 2) of work item `item` = (token, 256-rank pair).
+// Tiles (0, 1 or 2) of work item `item`: (token, 256-rank pair), or with
+// two-token items (tokens 2 item, 2 item + 1).
 __device__ __forceinline__ int sdi_ntiles(const SdiParams& p, int item) {
+    if (p.tt) return 2 * item + 1 < p.T ? 2 : 1;
     const int t = item / p.npairs, pr = item - t * p.npairs;
     if (p.cnt) {
         int m = __ldg(p.cnt + t);
@@ -244,11 +249,17 @@ __device__ __forceinline__ void store_staged_rows(const uint8_t* stage, uint16_t
     }
 }
 
-template <int H>
+template <int H, bool TT>
 struct SdiCfg {
+    static_assert(!TT || H <= 64, "two-token items need heads <= 64");
+    static constexpr int kTok = TT ? 2 : 1;                 // tokens per item
     static constexpr int kQBytes = H * 128;                 // H rows x 64 columns bf16
     static constexpr int kKvBytes = 128 * 128;              // 128 ranks x 64 columns bf16
-    static constexpr int kSlotBytes = 2 * kQBytes + 2 * kKvBytes;
+    // a slot: the item's q | dO (per token: q block then dO block) then the two
+    // kv tiles (A stage), or the item's 128-column q | dO blocks (B stage)
+    static constexpr int kKvOff = 2 * kQBytes * kTok;
+    static constexpr int kSlotA = kKvOff + 2 * kKvBytes, kSlotB = 4 * kQBytes * kTok;
+    static constexpr int kSlotBytes = kSlotA > kSlotB ? kSlotA : kSlotB;
     static constexpr int kSlotsRaw = 196608 / kSlotBytes;
     static constexpr int kSlots = kSlotsRaw > 8 ? 8 : kSlotsRaw;
     static constexpr int kThreads = 384;    // TMA, MMA, 8 epilogue warps, 2 copy warps
@@ -260,18 +271,18 @@ struct SdiCfg {
     static_assert(kSmem <= 232448, "shared memory of one CTA is at most 227 KB");
 };
 
-template <int H>
+template <int H, bool TT>
 __global__ void __launch_bounds__(384, 1)
 sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
            const __grid_constant__ CUtensorMap map_qda, const __grid_constant__ CUtensorMap map_qdb,
            const __grid_constant__ CUtensorMap map_im, const __grid_constant__ CUtensorMap map_ds,
            const SdiParams p) {
-    using C = SdiCfg<H>;
+    using C = SdiCfg<H, TT>;
     extern __shared__ uint8_t smem_raw[];
     SdiShared& sh = *reinterpret_cast<SdiShared*>(smem_raw);
     uint8_t* slots = align1024(smem_raw + sizeof(SdiShared));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nitems = p.T * p.npairs;
+    const int nitems = TT ? (p.T + 1) / 2 : p.T * p.npairs;
 
     if (threadIdx.x == 0) {
         // full: the TMA thread's arrive (with the q / dO bytes) + 64 copy threads
@@ -331,33 +342,42 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 if (last < nitems && !publish()) { ok = false; break; }
                 SMLA_TRACE_EV(0, it, 0);
                 SMLA_TRACE_VAL(0, it, 45, uint64_t(p.qd_mode));
-                const int t = item / p.npairs;
+                const int t = TT ? 2 * item : item / p.npairs;   // the item's first token
                 for (int c = 0; c < C::kUses; ++c) {
                     ok = wait_or_abort(&sh.empty[slot], phase ^ 1u, &sh.abort_flag, p.status);
                     if (!ok) break;
                     uint8_t* sb = slots + slot * C::kSlotBytes;
                     SMLA_TRACE_EV(0, it, 48 + c);
                     if (c < 8) {
-                        // A stage: q and dO columns [64c, 64c + 64)
-                        mbar_arrive_expect_tx(&sh.full[slot], 2 * C::kQBytes);
+                        // A stage: q and dO columns [64c, 64c + 64) of the item's token(s)
+                        mbar_arrive_expect_tx(&sh.full[slot], C::kKvOff);
                         if (p.qd_mode != 0) {
                             tma_load_5d(sb, &map_qda, 0, 0, c, 0, t, &sh.full[slot]);
                         } else {
-                            tma_load_2d(sb, &map_q, c * 64, t * H, &sh.full[slot]);
-                            tma_load_2d(sb + C::kQBytes, &map_do, c * 64, t * H, &sh.full[slot]);
+#pragma unroll
+                            for (int tk = 0; tk < C::kTok; ++tk) {
+                                tma_load_2d(sb + tk * 2 * C::kQBytes, &map_q, c * 64, (t + tk) * H, &sh.full[slot]);
+                                tma_load_2d(sb + tk * 2 * C::kQBytes + C::kQBytes, &map_do, c * 64, (t + tk) * H,
+                                            &sh.full[slot]);
+                            }
                         }
                     } else {
                         // B stage: q and dO columns [128b, 128b + 128), two 64-column
                         // blocks each; the copy warps skip these uses, so arrive for them.
                         const int b = c - 8;
-                        mbar_arrive_expect_tx(&sh.full[slot], 4 * C::kQBytes);
+                        mbar_arrive_expect_tx(&sh.full[slot], C::kSlotB);
                         if (p.qd_mode != 0) {
                             tma_load_5d(sb, &map_qdb, 0, 0, 2 * b, 0, t, &sh.full[slot]);
                         } else {
-                            tma_load_2d(sb, &map_q, b * 128, t * H, &sh.full[slot]);
-                            tma_load_2d(sb + C::kQBytes, &map_q, b * 128 + 64, t * H, &sh.full[slot]);
-                            tma_load_2d(sb + 2 * C::kQBytes, &map_do, b * 128, t * H, &sh.full[slot]);
-                            tma_load_2d(sb + 3 * C::kQBytes, &map_do, b * 128 + 64, t * H, &sh.full[slot]);
+#pragma unroll
+                            for (int tk = 0; tk < C::kTok; ++tk) {
+                                uint8_t* tb = sb + tk * 4 * C::kQBytes;
+                                const int row = (t + tk) * H;
+                                tma_load_2d(tb, &map_q, b * 128, row, &sh.full[slot]);
+                                tma_load_2d(tb + C::kQBytes, &map_q, b * 128 + 64, row, &sh.full[slot]);
+                                tma_load_2d(tb + 2 * C::kQBytes, &map_do, b * 128, row, &sh.full[slot]);
+                                tma_load_2d(tb + 3 * C::kQBytes, &map_do, b * 128 + 64, row, &sh.full[slot]);
+                            }
                         }
                         mbar_arrive_cnt(&sh.full[slot], 64);
                     }
@@ -386,17 +406,21 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         bool ok = true;
         int idx_cur[32], idx_nxt[32];
         auto load_idx = [&](int item, int (&out)[32]) {
-            const int t = item / p.npairs, pr = item - t * p.npairs;
+            // token and rank of row `row` (0..255, tile row >> 7) of the item
+            const int tok0 = TT ? 2 * item : item / p.npairs, tok1 = TT ? 2 * item + 1 : tok0;
+            const int rbase = TT ? 0 : (item - tok0 * p.npairs) * 256;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const int rl = pr * 256 + 8 * i + 4 * gw + (lane >> 3);
+                const int row = 8 * i + 4 * gw + (lane >> 3);
+                const int t = TT && row >= 128 ? tok1 : tok0;
+                const int rl = TT ? (row & 127) : rbase + row;
                 // masked, invalid, or past the chunk's end: any real row will do
                 // (P of that rank is zeroed), but not one fixed row, which every
                 // CTA would then read at once: the slot's own rank position
                 // spreads them over up to 512 rows (the zero-filling form of
                 // cp.async, and a modulo here, both measured slower)
                 int j = -1;
-                if (rl < p.R) {
+                if (rl < p.R && (!TT || t < p.T)) {
                     j = __ldg(p.topk + int64_t(t) * p.K + p.r0 + rl);
                     if (j < -1 || j >= p.N) { flag_status(p.status, SMLA_ERR_INDEX); j = -1; }
                 }
@@ -434,7 +458,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
-                uint8_t* kvb = slots + slot * C::kSlotBytes + 2 * C::kQBytes;
+                uint8_t* kvb = slots + slot * C::kSlotBytes + C::kKvOff;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int row = 8 * i + 4 * gw + (lane >> 3);   // 0..255 (tile = row >> 7)
@@ -511,11 +535,12 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                     tc_fence_after();
                     const uint32_t sb = smem_u32(slots + slot * C::kSlotBytes);
                     for (int g = 0; g < ntiles; ++g) {
-                        const uint32_t kvb = sb + 2 * C::kQBytes + g * C::kKvBytes;
+                        const uint32_t kvb = sb + C::kKvOff + g * C::kKvBytes;
+                        const uint32_t qdb = sb + (TT ? g * 2 * C::kQBytes : 0);   // the tile's token's q | dO
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             mma_ss(tbase + g * 256, sdesc_sw128(kvb + k * 32, 16, 1024),
-                                   sdesc_sw128(sb + k * 32, 16, 1024), C::kIdescA, (c | k) != 0);
+                                   sdesc_sw128(qdb + k * 32, 16, 1024), C::kIdescA, (c | k) != 0);
                         // tile 0's S^T | dP^T are complete one tile-step before tile 1's:
                         // its epilogue starts while tile 1's last MMAs run
                         if (c == 7) mma_commit(&sh.s_full[g]);
@@ -559,8 +584,10 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                             const bool pterm = ks < H / 16;
                             const int kk = pterm ? ks : ks - H / 16;
                             const uint32_t acol = kk * 16 + (pterm ? 0 : 8);
-                            // dO (P term) or q (dS term): two 64-column blocks of H rows
-                            const uint32_t bt = sb + (pterm ? do_off : q_off) + kk * 2048;
+                            // dO (P term) or q (dS term) of the tile's token: two 64-column
+                            // blocks of H rows
+                            const uint32_t bt = sb + (TT ? g * 4 * C::kQBytes : 0) + (pterm ? do_off : q_off) +
+                                                kk * 2048;
                             mma_ts(tile + 128, tile + acol, sdesc_sw128(bt, C::kQBytes, 1024),
                                    C::kIdescB, ks != 0);
                         }
@@ -599,8 +626,10 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
         const int quarter = warp & 3;                   // TMEM lane quarter of this warp
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
         uint8_t* stage = slots + C::kSlots * C::kSlotBytes + (warp - 2) * kStageBytes;
-        float* lsd = reinterpret_cast<float*>(stage);   // [0, H): -lse*log2(e); [H, 2H): -scale*delta
-        static_assert(2 * H * 4 <= kStageBytes, "lse / delta must fit the staging tile");
+        // per token of the item (at 2H k for its k-th token): [0, H): -lse*log2(e);
+        // [H, 2H): -scale*delta
+        float* lsd = reinterpret_cast<float*>(stage);
+        static_assert(2 * H * 4 * C::kTok <= kStageBytes, "lse / delta must fit the staging tile");
         constexpr int kChunks = H / 16;                 // 16-head chunks
         constexpr int kSplit = (kChunks + 1) / 2;       // group 0's chunks: [0, kSplit)
         const float c1 = p.scale * kLog2e;
@@ -618,15 +647,24 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             const int ent = queue_read_warp(sh, it, p.status, qok);
             const int item = ent >> 2;
             if (!qok || item >= nitems) break;
-            const int t = item / p.npairs, pr = item - t * p.npairs;
             const int ntiles = ent & 3;
+            // the item's first token and its rank pair (one token per item unless TT)
+            const int t = TT ? 2 * item : item / p.npairs, pr = TT ? 0 : item - t * p.npairs;
+            auto tok_of = [&](int g) { return TT ? t + g : t; };
+            auto rank0_of = [&](int g) { return TT ? 0 : pr * 256 + g * 128; };
             // lane l holds -lse * log2(e) and -scale * delta of heads l, l + 32, ...
-            float lse_w[kHw], del_w[kHw];
+            // of each of the item's tokens
+            float lse_w[C::kTok][kHw], del_w[C::kTok][kHw];
 #pragma unroll
-            for (int k = 0; k < kHw; ++k) {
-                const int h = k * 32 + lane;
-                lse_w[k] = h < H ? -(__ldg(p.lse + int64_t(t) * H + h) * kLog2e) : 0.f;
-                del_w[k] = h < H ? -(p.scale * __ldg(p.delta + int64_t(t) * H + h)) : 0.f;
+            for (int tk = 0; tk < C::kTok; ++tk) {
+                const int tt = t + tk;
+#pragma unroll
+                for (int k = 0; k < kHw; ++k) {
+                    const int h = k * 32 + lane;
+                    const bool in = h < H && (!TT || tt < p.T);
+                    lse_w[tk][k] = in ? -(__ldg(p.lse + int64_t(tt) * H + h) * kLog2e) : 0.f;
+                    del_w[tk][k] = in ? -(p.scale * __ldg(p.delta + int64_t(tt) * H + h)) : 0.f;
+                }
             }
             // -lse * log2(e) and -scale * delta of every head go to the head of this
             // warp's staging tile (free once its last TMA store has read it), from
@@ -634,18 +672,22 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
 #pragma unroll
-            for (int k = 0; k < kHw; ++k) {
-                const int h = k * 32 + lane;
-                if (h < H) { lsd[h] = lse_w[k]; lsd[H + h] = del_w[k]; }
-            }
+            for (int tk = 0; tk < C::kTok; ++tk)
+#pragma unroll
+                for (int k = 0; k < kHw; ++k) {
+                    const int h = k * 32 + lane;
+                    if (h < H) { lsd[2 * H * tk + h] = lse_w[tk][k]; lsd[2 * H * tk + H + h] = del_w[tk][k]; }
+                }
             __syncwarp();
             bool ok = true;
             // ---- P and scale*dS of each tile, written back into TMEM as bf16 pairs
             for (int g2 = 0; g2 < ntiles && ok; ++g2) {
-                const int rl = pr * 256 + g2 * 128 + quarter * 32 + lane;   // this lane's rank
+                const int tg = tok_of(g2);
+                const int rl = rank0_of(g2) + quarter * 32 + lane;   // this lane's rank
+                const float* lsdg = lsd + (TT ? 2 * H * g2 : 0);
                 bool valid = false;
                 if (rl < p.R) {
-                    const int j = __ldg(p.topk + int64_t(t) * p.K + p.r0 + rl);
+                    const int j = __ldg(p.topk + int64_t(tg) * p.K + p.r0 + rl);
                     valid = j >= 0 && j < p.N;
                 }
                 const uint32_t sphase = (g2 ? s_seen1 : s_seen0) & 1u;
@@ -683,8 +725,8 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                             float2 nl[8], nd[8];
 #pragma unroll
                             for (int v = 0; v < 4; ++v) {
-                                const float4 a = reinterpret_cast<const float4*>(lsd + k * 16)[v];
-                                const float4 b = reinterpret_cast<const float4*>(lsd + H + k * 16)[v];
+                                const float4 a = reinterpret_cast<const float4*>(lsdg + k * 16)[v];
+                                const float4 b = reinterpret_cast<const float4*>(lsdg + H + k * 16)[v];
                                 nl[2 * v] = make_float2(a.x, a.y); nl[2 * v + 1] = make_float2(a.z, a.w);
                                 nd[2 * v] = make_float2(b.x, b.y); nd[2 * v + 1] = make_float2(b.z, b.w);
                             }
@@ -742,7 +784,8 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 const uint32_t pphase = ((g2 ? p_arr1 : p_arr0) - 1u) & 1u;
                 if (!wait_or_abort_warp(&sh.p_ready[g2], pphase, &sh.abort_flag, p.status)) return false;
                 tc_fence_after();
-                const int row0 = pr * 256 + g2 * 128 + quarter * 32;   // first rank of these rows
+                const int tg = tok_of(g2);
+                const int row0 = rank0_of(g2) + quarter * 32;   // first rank of these rows
                 const uint32_t trow = tbase + lane_off + g2 * 256;
                 uint32_t dsw[32];
 #pragma unroll
@@ -764,7 +807,7 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(&map_ds, grp * 64, t * p.ds_rows + p.ds_off + row0, stage);
+                    tma_store_2d(&map_ds, grp * 64, tg * p.ds_rows + p.ds_off + row0, stage);
                     bulk_commit();
                 }
                 __syncwarp();
@@ -807,19 +850,20 @@ sdi_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CU
 #pragma unroll
                     for (int v = 0; v < 4; ++v) srow[(v + 4) ^ (lane & 7)] = pack8(v1 + 8 * v);
                     const int col = 128 * c + 64 * grp;
-                    const int drow0 = pr * 256 + g2 * 128 + quarter * 32;   // first rank of these rows
+                    const int tg = tok_of(g2);
+                    const int drow0 = rank0_of(g2) + quarter * 32;   // first rank of these rows
                     if (drow0 + 32 <= p.R) {
                         // the warp's 32 ranks all belong to this chunk: one TMA store
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(&map_im, col, t * p.R + drow0, stage);
+                            tma_store_2d(&map_im, col, tg * p.R + drow0, stage);
                             bulk_commit();
                         }
                     } else {
                         // ragged last rows: plain stores of the rows < R
                         __syncwarp();
-                        store_staged_rows(stage, p.interm + (int64_t(t) * p.R + drow0) * kD + col, kD,
+                        store_staged_rows(stage, p.interm + (int64_t(tg) * p.R + drow0) * kD + col, kD,
                                           p.R - drow0, lane);
                     }
                     __syncwarp();
@@ -1182,11 +1226,11 @@ int set_smem_attrs_once(const void* fn, int smem, bool* done) {
     return 0;
 }
 
-template <int H>
-cudaError_t launch_sdi_h(const ChunkArgs& a, cudaStream_t s) {
-    using C = SdiCfg<H>;
+template <int H, bool TT>
+cudaError_t launch_sdi_hh(const ChunkArgs& a, cudaStream_t s) {
+    using C = SdiCfg<H, TT>;
     static bool attr_done[64] = {false};
-    if (set_smem_attrs_once(reinterpret_cast<const void*>(sdi_kernel<H>), C::kSmem, attr_done))
+    if (set_smem_attrs_once(reinterpret_cast<const void*>(sdi_kernel<H, TT>), C::kSmem, attr_done))
         return cudaErrorInvalidValue;
     const int Rp = round_up_ranks(a.R), Hp = pad_heads(H);
     CUtensorMap mq, mdo, mqda, mqdb, mim, mds;
@@ -1198,8 +1242,8 @@ cudaError_t launch_sdi_h(const ChunkArgs& a, cudaStream_t s) {
         const bool q_first = uq < ud;
         const void* lo = q_first ? static_cast<const void*>(a.q) : static_cast<const void*>(a.dO);
         const uint64_t dist = q_first ? uint64_t(ud - uq) : uint64_t(uq - ud);
-        if (make_tmap_bf16_pair5d(&mqda, lo, dist, uint64_t(a.T), H, 1) &&
-            make_tmap_bf16_pair5d(&mqdb, lo, dist, uint64_t(a.T), H, 2))
+        if (make_tmap_bf16_pair5d(&mqda, lo, dist, uint64_t(a.T), H, 1, C::kTok) &&
+            make_tmap_bf16_pair5d(&mqdb, lo, dist, uint64_t(a.T), H, 2, C::kTok))
             qd_mode = q_first ? 1 : 2;
         else
             mqda = mqdb = CUtensorMap{};
@@ -1220,14 +1264,26 @@ cudaError_t launch_sdi_h(const ChunkArgs& a, cudaStream_t s) {
     sp.qd_mode = qd_mode;
     sp.work_ctr = sdi_work_counter(a.status);
     sp.cnt = a.cnt;
-    const int64_t items = int64_t(a.T) * sp.npairs;
+    sp.tt = TT ? 1 : 0;
+    const int64_t items = TT ? (int64_t(a.T) + 1) / 2 : int64_t(a.T) * sp.npairs;
     const int sms = sm_count();
     const int grid = int(items < sms ? items : sms);
     cudaError_t e = cudaMemsetAsync(sp.work_ctr, 0, sizeof(int), s);
     if (e != cudaSuccess) return e;
-    sdi_kernel<H><<<grid, C::kThreads, C::kSmem, s>>>(mq, mdo, mqda, mqdb, mim, mds, sp);
+    sdi_kernel<H, TT><<<grid, C::kThreads, C::kSmem, s>>>(mq, mdo, mqda, mqdb, mim, mds, sp);
     note_launch();
     return cudaGetLastError();
+}
+
+// Two-token items when a token has at most one tile (chunks of at most 128
+// ranks) and a ring slot holds two tokens' q and dO (heads <= 64): the B
+// stage then alternates tiles again, and each TMA box serves two tokens.
+template <int H>
+cudaError_t launch_sdi_h(const ChunkArgs& a, cudaStream_t s) {
+    if constexpr (H <= 64) {
+        if (a.R <= 128) return launch_sdi_hh<H, true>(a, s);
+    }
+    return launch_sdi_hh<H, false>(a, s);
 }
 
 template <int H>

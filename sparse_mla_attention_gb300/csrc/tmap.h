@@ -49,19 +49,20 @@ inline bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, u
 // innermost first: column inside a 64-column block (64), head (H, stride one
 // row), 64-column block (8, stride 128 bytes), which tensor (2, stride
 // `pair_stride_bytes` = address of b minus address of a) and token (T, stride
-// H rows). A box of `blocks` column blocks of both tensors for one token lands
-// in shared memory as [tensor][block][head][64 columns], 128-byte swizzled, the
-// same bytes as 2 x `blocks` separate [H x 64] boxes laid end to end. Returns
-// false if the driver refuses the encoding (e.g. a stride of 2^40 bytes or more).
+// H rows). A box of `blocks` column blocks of both tensors for `tokens`
+// consecutive tokens lands in shared memory as [token][tensor][block][head][64
+// columns], 128-byte swizzled, the same bytes as separate [H x 64] boxes laid
+// end to end (a token past T reads zeros). Returns false if the driver refuses
+// the encoding (e.g. a stride of 2^40 bytes or more).
 inline bool make_tmap_bf16_pair5d(CUtensorMap* m, const void* a, uint64_t pair_stride_bytes,
-                                  uint64_t T, uint32_t H, uint32_t blocks) {
+                                  uint64_t T, uint32_t H, uint32_t blocks, uint32_t tokens = 1) {
     auto fn = encode_tiled_fn();
     if (!fn) return false;
     if (pair_stride_bytes == 0 || pair_stride_bytes % 16 != 0 || pair_stride_bytes >= (uint64_t(1) << 40))
         return false;
     cuuint64_t dims[5] = {64, H, 8, 2, T};
     cuuint64_t strides[4] = {1024, 128, pair_stride_bytes, uint64_t(H) * 1024};
-    cuuint32_t box[5] = {64, H, blocks, 2, 1};
+    cuuint32_t box[5] = {64, H, blocks, 2, tokens};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(a), dims, strides, box,
                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -233,6 +233,8 @@ def test_bwd_t1024_chunked_matches_unchunked(t1024):
     (80, 64, 90, 33, False, 32),    # 64-head stash padding (48), 128-head padding
     (96, 256, 300, 160, True, 128), # (80, 96, 112), more tokens than SMs (160)
     (112, 130, 200, 21, True, 0),
+    (48, 100, 150, 41, True, 0),    # two-token items (heads <= 64, <= 128 ranks), odd T:
+    (16, 256, 300, 33, False, 64),  # the last item has one token; unchunked and chunked
 ])
 def test_bwd_custom_shapes(H, K, N, T, sink, chunk):
     c = Case(custom_inputs(H * 7 + K, T=T, H=H, K=K, N=N, sink=sink,
@@ -268,6 +270,24 @@ def test_bwd_q_do_placement(H, K, N, T):
     compare("dq (dO = q)", to_f64(dq), ref2["dq"])
     compare("dkv (dO = q)", to_f64(dkv), ref2["dkv"])
     compare("d_sink (dO = q)", to_f64(ds), ref2["dsink"])
+
+
+def test_bwd_valid_counts_on_tile_boundaries():
+    """Each token's valid ranks are compacted before tiling: counts of 0, 1 and
+    around every 64-rank chunk and 128-rank tile boundary, masked slots at
+    random positions, duplicate indices kept."""
+    counts = [0, 1, 2, 63, 64, 65, 127, 128, 129, 191, 192, 255, 256, 257, 300, 383, 384, 385, 400]
+    T, H, K, N = len(counts), 64, 400, 700
+    c = custom_inputs(991, T=T, H=H, K=K, N=N, sink=True, mask_p=0.0)
+    rng = np.random.default_rng(991)
+    topk = c["topk"]
+    for t, m in enumerate(counts):
+        keep = np.zeros(K, dtype=bool)
+        keep[rng.choice(K, size=m, replace=False)] = True
+        topk[t, ~keep] = -1
+    topk[3, np.flatnonzero(topk[3] >= 0)[:2]] = 5      # a duplicated row inside a token
+    case = Case(c)
+    _check_full(case)
 
 
 def test_bwd_empty_T():
