@@ -558,11 +558,11 @@ OVERLAPPED_PHASES = ("csr", "attn_dq", "gather")
 # DRAM traffic per launch of the dominant kernels, from one ncu capture (see
 # profiles/), valid only while the kernel source is the one captured.
 _NCU_TRAFFIC = {
-    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "8064850532842318"),
-                 "bytes_per_token": (139.401728e6 + 275.856896e6) / 512,
+    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "3048d7bc0b5fe44f"),
+                 "bytes_per_token": (140.994560e6 + 275.396608e6) / 512,
                  "note": "ncu capture of the first 512 tokens, scaled by tokens"},
-    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "8064850532842318"),
-                "bytes_per_token": (69.763328e6 + 17.347328e6) / 512,
+    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "3048d7bc0b5fe44f"),
+                "bytes_per_token": (68.704000e6 + 17.142528e6) / 512,
                 "note": "ncu capture of the first 512 tokens, scaled by tokens"},
     "fwd_tc": {"sources": ("sparse_mla_attention_gb300/csrc/k_fwd_tc.cu", "9782f171a5790295"),
                "bytes_per_token": (72.783872e6 + 17.696512e6) / 512,
