@@ -242,6 +242,23 @@ def test_bwd_custom_shapes(H, K, N, T, sink, chunk):
     _check_full(c, r_chunk=chunk or None)
 
 
+@pytest.mark.parametrize("H,K,N,T,sink,chunk,mask_p", [
+    (128, 512, 700, 45, True, 0, 0.1),     # two 256-rank items per token, masked slots compacted
+    (128, 600, 900, 23, True, 0, 0.0),     # a third, ragged item (88 ranks)
+    (64, 384, 500, 50, False, 0, 0.3),     # the second item has one tile
+    (96, 520, 640, 31, True, 0, 0.05),     # 8 ranks in the third item
+    (128, 640, 800, 17, True, 320, 0.1),   # two rank chunks of 320 (per-chunk dq)
+    (112, 257, 300, 40, False, 0, 0.0),    # one rank past two tiles
+])
+def test_bwd_many_rank_items(H, K, N, T, sink, chunk, mask_p):
+    """Tokens with more than 256 ranks (per chunk) span several S/dP/dS items:
+    ragged last items, items of one tile or a few ranks, masked slots that
+    compaction moves to the end, and rank chunks wider than 256."""
+    c = Case(custom_inputs(H * 5 + K, T=T, H=H, K=K, N=N, sink=sink, mask_p=mask_p,
+                           all_masked_rows=(min(3, T - 1),), r_chunk=chunk))
+    _check_full(c, r_chunk=chunk or None)
+
+
 @pytest.mark.parametrize("H,K,N,T", [(64, 200, 260, 130), (128, 300, 400, 20)])
 def test_bwd_q_do_placement(H, K, N, T):
     """q and dO are fetched as one paired tensor when one sits below the other
