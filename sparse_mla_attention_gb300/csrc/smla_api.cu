@@ -3,7 +3,8 @@
 //
 // Phase order follows the aiter page "Sparse MLA training backward"
 // (Structure table): delta, then per rank chunk (R_CHUNK) the CSR build, the
-// dQ / dKV-interm work and the atomic-free dKV gather, then d_sink. The
+// dQ / dKV-interm work and the atomic-free dKV gather, then d_sink (which
+// needs only delta and lse, and runs on the side stream under the gather). The
 // validation rules are the page wrapper's (D == 512, num_kv >= T, shapes),
 // plus the review comments on that page (R_CHUNK must divide topk; dtype and
 // lse shape checks), plus alignment and overlap checks.
@@ -359,13 +360,16 @@ int enqueue_bwd(const BwdArgs& A, const smla_dims& d, const BwdPlan& plan, char*
             if ((rc = cuda_rc(cudaStreamWaitEvent(s, side->dq_done, 0)))) return rc;
         }
     }
-    // the caller's stream waits for the last dq
+    // d_sink needs only delta and lse: on the side stream after the last dq
+    // (delta precedes every S/dP/dS launch whose completion the side stream
+    // waited for), so that it runs under the gather's tail instead of after it;
+    // the caller's stream then waits for both
+    if (A.sink) {
+        prof::Scope ph(prof::kDsink, side->stream);
+        if ((rc = cuda_rc(launch_dsink(delta, A.lse, A.sink, A.d_sink, d.T, d.H, side->stream)))) return rc;
+    }
     if ((rc = cuda_rc(cudaEventRecord(side->dq_done, side->stream)))) return rc;
     if ((rc = cuda_rc(cudaStreamWaitEvent(s, side->dq_done, 0)))) return rc;
-    if (A.sink) {
-        prof::Scope ph(prof::kDsink, s);
-        if ((rc = cuda_rc(launch_dsink(delta, A.lse, A.sink, A.d_sink, d.T, d.H, s)))) return rc;
-    }
     return SMLA_OK;
 }
 
