@@ -930,13 +930,16 @@ constexpr int kDqThreads = (6 + kDqCopyWarps) * 32;         // TMA, MMA, 4 epilo
 constexpr int kDqABytes = 2 * 64 * 128;        // two 64-head blocks x 64 ranks
 constexpr int kDqBBytes = 4 * 64 * 128;        // four 64-column blocks x 64 ranks
 constexpr int kDqSlotBytes = kDqABytes + kDqBBytes;
-constexpr int kDqSmem = int(sizeof(DqShared)) + 1024 + kDqSlots * kDqSlotBytes;
+// Per epilogue warp, two 32-row x 128-byte staging tiles for the TMA stores of bf16 dq.
+constexpr int kDqStageBytes = 4 * 2 * kStageBytes;
+constexpr int kDqSmem = int(sizeof(DqShared)) + 1024 + kDqSlots * kDqSlotBytes + kDqStageBytes;
 static_assert(kDqSmem <= 232448, "shared memory of one CTA is at most 227 KB");
 constexpr uint32_t kDqIdesc = idesc_bf16(128, 256, true, true);
 
 template <int H>
 __global__ void __launch_bounds__(kDqThreads, 1)
-dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
+dq_kernel(const __grid_constant__ CUtensorMap map_ds, const __grid_constant__ CUtensorMap map_dq,
+          const DqParams p) {
     extern __shared__ uint8_t smem_raw[];
     DqShared& sh = *reinterpret_cast<DqShared*>(smem_raw);
     uint8_t* slots = align1024(smem_raw + sizeof(DqShared));
@@ -1107,6 +1110,13 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
         const int quarter = warp & 3;
         const int h = quarter * 32 + lane;
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+        // bf16 dq without an fp32 accumulator, whole 32-head quarters: each warp
+        // stages 64 columns of its 32 heads (one row per lane, 128-byte
+        // swizzle) and writes them with one TMA store; per-lane 16-byte stores
+        // touch 32 rows per instruction instead
+        constexpr bool kTmaOut = H % 32 == 0;
+        const bool tma_out = kTmaOut && p.dq_acc == nullptr;
+        uint8_t* stage = slots + kDqSlots * kDqSlotBytes + (warp - 2) * 2 * kStageBytes;
         int it = 0;
         for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++it) {
             const int t = item >> 1, half = item & 1;
@@ -1121,7 +1131,27 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
                 uint32_t v[32];
                 tmem_ld32(tbase + lane_off + 256 * b + 32 * c, v);
                 tmem_wait_ld();
-                if (h < H) {
+                if (tma_out) {
+                    if (quarter * 32 < H) {
+                        uint8_t* st = stage + ((c >> 1) & 1) * kStageBytes;
+                        // the staging tile's previous store (two stores ago) has been read
+                        if ((c & 1) == 0) {
+                            if (lane == 0) bulk_wait_read_1();
+                            __syncwarp();
+                        }
+                        uint4* srow = reinterpret_cast<uint4*>(st + lane * 128);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) srow[((c & 1) * 4 + k) ^ (lane & 7)] = pack8(v + 8 * k);
+                        if (c & 1) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&map_dq, half * 256 + (c >> 1) * 64, t * H + quarter * 32, st);
+                                bulk_commit();
+                            }
+                        }
+                    }
+                } else if (h < H) {
                     float f[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(v[k]);
@@ -1156,6 +1186,8 @@ dq_kernel(const __grid_constant__ CUtensorMap map_ds, const DqParams p) {
             if (lane == 0) mbar_arrive(&sh.d_empty[b]);
             if (warp == 2 && lane == 0) SMLA_TRACE_EV(1, it, 5);
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -1292,8 +1324,12 @@ cudaError_t launch_dq_h(const ChunkArgs& a, cudaStream_t s) {
     if (set_smem_attrs_once(reinterpret_cast<const void*>(dq_kernel<H>), kDqSmem, attr_done))
         return cudaErrorInvalidValue;
     const int Rp = round_up_ranks(a.R), Hp = pad_heads(H);
-    CUtensorMap mds;
+    CUtensorMap mds, mdq = CUtensorMap{};
     if (!make_tmap_bf16_2d(&mds, a.dsT, uint64_t(a.T) * Rp, Hp, Hp, 64, 64, true))
+        return cudaErrorInvalidValue;
+    // bf16 dq rows in boxes of 32 heads x 64 columns (whole 32-head quarters only)
+    if (H % 32 == 0 && !a.dq_acc &&
+        !make_tmap_bf16_2d(&mdq, a.dq_out, uint64_t(a.T) * H, kD, kD, 32, 64, true))
         return cudaErrorInvalidValue;
     DqParams dp{};
     dp.kv = a.kv; dp.topk = a.topk; dp.dq_acc = a.dq_acc; dp.dq_out = a.dq_out;
@@ -1308,7 +1344,7 @@ cudaError_t launch_dq_h(const ChunkArgs& a, cudaStream_t s) {
     // 96, 104, 114, 120 and 128 CTAs measured 1.94, 1.92, 1.91, 1.90, 1.90).
     const int sms = (sm_count() * 4) / 5 > 0 ? (sm_count() * 4) / 5 : 1;
     const int grid = int(items < sms ? items : sms);
-    dq_kernel<H><<<grid, kDqThreads, kDqSmem, s>>>(mds, dp);
+    dq_kernel<H><<<grid, kDqThreads, kDqSmem, s>>>(mds, mdq, dp);
     note_launch();
     return cudaGetLastError();
 }
