@@ -558,11 +558,11 @@ OVERLAPPED_PHASES = ("csr", "attn_dq", "gather")
 # DRAM traffic per launch of the dominant kernels, from one ncu capture (see
 # profiles/), valid only while the kernel source is the one captured.
 _NCU_TRAFFIC = {
-    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "3048d7bc0b5fe44f"),
-                 "bytes_per_token": (140.994560e6 + 275.396608e6) / 512,
+    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "2d8bc6c49d1125e9"),
+                 "bytes_per_token": (140.994816e6 + 275.318272e6) / 512,
                  "note": "ncu capture of the first 512 tokens, scaled by tokens"},
-    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "3048d7bc0b5fe44f"),
-                "bytes_per_token": (68.704000e6 + 17.142528e6) / 512,
+    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "2d8bc6c49d1125e9"),
+                "bytes_per_token": (68.702208e6 + 23.128832e6) / 512,
                 "note": "ncu capture of the first 512 tokens, scaled by tokens"},
     "fwd_tc": {"sources": ("sparse_mla_attention_gb300/csrc/k_fwd_tc.cu", "1debdf8c27880f41"),
                "bytes_per_token": (73.644544e6 + 18.696448e6) / 512,

@@ -1338,11 +1338,14 @@ cudaError_t launch_dq_h(const ChunkArgs& a, cudaStream_t s) {
     dp.cnt = a.cnt;
     const int64_t items = int64_t(a.T) * 2;
     // dq runs beside the dKV gather (another stream). Each dq CTA's throughput
-    // is fixed by its own copy pipeline, while the gather speeds up with every
-    // SM it gets: on 4/5 of the SMs the two finish sooner together (T=4096,
-    // H=128, topk=512: 1.90 ms per backward against 1.95 ms on all 152 SMs;
-    // 96, 104, 114, 120 and 128 CTAs measured 1.94, 1.92, 1.91, 1.90, 1.90).
-    const int sms = (sm_count() * 4) / 5 > 0 ? (sm_count() * 4) / 5 : 1;
+    // is fixed by its own pipeline, while the gather speeds up with every SM it
+    // gets, so dq takes the share of the SMs at which both end together. Beside
+    // a whole gather (T=4096, H=128, topk=512): 96 of 152 SMs, 1.809 ms per
+    // backward against 1.833 / 1.816 / 1.819 / 1.829 / 1.829 ms with 88 / 104 /
+    // 112 / 121 / 136 (dq ends last below 96). Beside the last rank chunk's
+    // gather only (rank chunks, dq over all ranks at the end): 4/5 of the SMs.
+    const int share = a.dq_beside_part ? (sm_count() * 4) / 5 : (sm_count() * 96) / 152;
+    const int sms = share > 0 ? share : 1;
     const int grid = int(items < sms ? items : sms);
     dq_kernel<H><<<grid, kDqThreads, kDqSmem, s>>>(mds, mdq, dp);
     note_launch();

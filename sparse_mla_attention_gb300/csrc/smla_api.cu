@@ -329,6 +329,7 @@ int enqueue_bwd(const BwdArgs& A, const smla_dims& d, const BwdPlan& plan, char*
             // chunks precede it on that stream, so the dq accumulator keeps its order)
             if (!plan.full_stash || last) {
                 ChunkArgs b = a;
+                b.dq_beside_part = plan.nchunks > 1;
                 if (plan.full_stash) {
                     // dq over all ranks from the full stash, once
                     b.r0 = 0; b.R = int(plan.K); b.ds_off = 0;

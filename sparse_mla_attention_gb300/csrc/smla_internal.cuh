@@ -158,6 +158,8 @@ struct ChunkArgs {
     int ds_rows, ds_off;
     float* dq_acc; uint16_t* dq_out;   // dq_acc NULL when unchunked
     bool first_chunk, last_chunk;
+    // dq runs beside only part of the dKV gather (rank chunks): it gets more SMs
+    bool dq_beside_part;
     unsigned* status;
 };
 // The two tensor-core kernels of one chunk: S/dP/P/dS + interm (+ dS stash),
