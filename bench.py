@@ -558,10 +558,10 @@ OVERLAPPED_PHASES = ("csr", "attn_dq", "gather")
 # DRAM traffic per launch of the dominant kernels, from one ncu capture (see
 # profiles/), valid only while the kernel source is the one captured.
 _NCU_TRAFFIC = {
-    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "2d8bc6c49d1125e9"),
+    "attn_sdi": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "c0d38424e2c5da67"),
                  "bytes_per_token": (140.994816e6 + 275.318272e6) / 512,
                  "note": "ncu capture of the first 512 tokens, scaled by tokens"},
-    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "2d8bc6c49d1125e9"),
+    "attn_dq": {"sources": ("sparse_mla_attention_gb300/csrc/k_attn_tc.cu", "c0d38424e2c5da67"),
                 "bytes_per_token": (68.702208e6 + 23.128832e6) / 512,
                 "note": "ncu capture of the first 512 tokens, scaled by tokens"},
     "fwd_tc": {"sources": ("sparse_mla_attention_gb300/csrc/k_fwd_tc.cu", "1debdf8c27880f41"),

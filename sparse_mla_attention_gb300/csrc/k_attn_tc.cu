@@ -35,8 +35,9 @@
 // dq_kernel: persistent; item = (token, half of D). dq = (scale*dS) x kv:
 // M = 128 (heads, zero-padded), N = 256, K = ranks in 64-rank steps, both
 // operands MN-major (scale*dS^T rows by TMA from the stash, kv rows gathered
-// by four copy warps), accumulated in TMEM (two 256-column buffers) and
-// written as bf16 (or added to an fp32 accumulator between rank chunks).
+// by eight copy warps in two teams), accumulated in TMEM (two 256-column
+// buffers) and written as bf16 through shared memory by TMA stores (or added
+// to an fp32 accumulator between rank chunks).
 //
 // Every mbarrier wait is bounded (kWaitNs); a timeout sets SMLA_ERR_TIMEOUT in
 // the status word, stops the CTA's loops, waits (bounded) for its own copies
