@@ -82,7 +82,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int
         : "memory");
 }
 
-// Prefetch one box of a 2-D tiled tensor into L2 (no shared-memory destination).
 // 5-D tiled load of one box into smem at coordinates (c0 .. c4), completing
 // on the mbarrier's transaction count.
 __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* m, int c0, int c1, int c2,
@@ -95,6 +94,7 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* m, int
         : "memory");
 }
 
+// Prefetch one box of a 2-D tiled tensor into L2 (no shared-memory destination).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                      reinterpret_cast<uint64_t>(m)),
